@@ -1,0 +1,512 @@
+"""Benchmark of the paged-KV GQA attention hot path on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-extra]
+
+A step is one pass of the hot path over one batch of synthetic input.  For a
+decode workload: RoPE of the new tokens' Q/K + append of their K/V through
+slot_mapping (pa_rope_kv_write) and decode attention of every sequence
+against its whole cache (pa_decode).  For the prefill workload: RoPE + append
+of the new tokens and varlen causal prefill reading the cached prefix
+through block_tables (pa_prefill_varlen).
+
+The headline workload is the Llama-2-7B-shaped MHA decode (32 heads, d=128,
+batch 32, 2048 cached tokens + 1); its metric is decode throughput in GB/s of
+KV bytes read (sum of context lengths x n_kv_heads x head_dim x 2 (K, V) x 2 B).
+The line also carries the other workloads (GQA decode, ragged decode,
+prefill in TFLOP/s) under "per_workload" unless --no-extra.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier +
+synchronize on each side, CUDA events on the launching stream; the KV cache
+(>= 1 GB) is larger than the 129 MB L2, so nothing is served from L2 across
+steps.  Per-kernel durations of the dominant kernel come from events around
+its launches inside the same timed loop.  `e2e` repeats the step through the
+same C-ABI calls with the step's inputs copied from pinned host memory and
+the output copied back inside the timed region.
+
+--impl reference times the CPU oracle (the only implementation the source
+pages define) on a bounded sample of the same workload.  Under torchrun with
+N > 1 every rank runs the same workload on its own GPU (replicas; the path
+has no exchange step) and rank 0 prints one line with the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_rope_gb300 import workloads as W  # noqa: E402
+
+HEADLINE = "mha_decode_7b"
+METRIC = "paged GQA decode KV GB/s (% of HBM peak); prefill attention TFLOP/s (% peak)"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- work units
+
+def kv_bytes(case) -> int:
+    wl = case.wl
+    ctx = case.num_cached.astype(np.int64) + 1
+    return int(ctx.sum()) * wl.n_kv_heads * wl.head_dim * 2 * 2
+
+
+def prefill_flops(case) -> int:
+    wl = case.wl
+    tot = 0
+    for p, n in zip(case.num_cached.tolist(), case.num_new.tolist()):
+        tot += n * (p + 1) + n * (n - 1) // 2
+    return 4 * wl.head_dim * wl.n_heads * tot
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.err = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception as e:  # nvidia-smi missing
+            self.err = str(e)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.err or not self.lines:
+            return {"error": self.err or "no samples"}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"error": "unparsed samples"}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class DecodeBench:
+    def __init__(self, name, dev):
+        import torch
+        from paged_kv_gqa_rope_gb300 import pa
+        self.pa, self.torch = pa, torch
+        case = W.make_case(name)
+        self.case = case
+        wl = case.wl
+        md = pa.prepare_decode(case.num_cached, case.block_tables)
+        self.md = md
+        self.table = pa.rope_table(int(md["positions"].max()) + 1, wl.head_dim, wl.rope_theta)
+        self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
+        self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
+        self.host = dict(q=case.q, k=case.k, v=case.v, positions=md["positions"],
+                         slots=md["slot_mapping"], bt=case.block_tables, ctx=md["context_lens"])
+        self.d = {k_: t(v_) for k_, v_ in self.host.items()}
+        self.ws = pa.decode_workspace(len(case.num_cached), wl.n_heads, wl.n_kv_heads,
+                                      wl.head_dim, int(md["context_lens"].sum()), device=dev)
+        self.out = torch.empty_like(self.d["q"])
+        self.status = pa.new_status(dev)
+        self.units = kv_bytes(case)
+        self.unit = "GB/s"
+        self.launches_per_step = 2
+
+    def step(self, ev=None):
+        pa, d, wl = self.pa, self.d, self.case.wl
+        pa.rope_kv_write(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
+                         self.cache, status=self.status)
+        if ev is not None:
+            ev[0].record()
+        pa.decode(d["q"], self.cache, d["bt"], d["ctx"], self.ws, wl.n_kv_heads, out=self.out,
+                  status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.pinned = {k_: torch.from_numpy(np.ascontiguousarray(v_)).pin_memory()
+                       for k_, v_ in self.host.items()}
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v_.numel() * v_.element_size() for v_ in self.pinned.values())
+        return h2d, self.out_host.numel() * self.out_host.element_size()
+
+    def e2e_step(self):
+        for k_, v_ in self.pinned.items():
+            self.d[k_].copy_(v_, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def kernel_name(self):
+        return "decode_kernel"
+
+
+class PrefillBench:
+    def __init__(self, name, dev):
+        import torch
+        from paged_kv_gqa_rope_gb300 import pa
+        self.pa, self.torch = pa, torch
+        case = W.make_case(name)
+        self.case = case
+        wl = case.wl
+        md = pa.prepare_prefill(case.num_cached, case.num_new, case.block_tables)
+        self.md = md
+        self.table = pa.rope_table(int(md["max_seqlen_k"]), wl.head_dim, wl.rope_theta)
+        self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
+        self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
+        self.host = dict(q=case.q, k=case.k, v=case.v, positions=md["positions"],
+                         slots=md["slot_mapping"], bt=case.block_tables,
+                         cuq=md["cu_seqlens_q"], cuk=md["cu_seqlens_k"])
+        self.d = {k_: t(v_) for k_, v_ in self.host.items()}
+        self.out = torch.empty_like(self.d["q"])
+        self.status = pa.new_status(dev)
+        self.units = prefill_flops(case)
+        self.unit = "TFLOP/s"
+        self.launches_per_step = 2
+
+    def step(self, ev=None):
+        pa, d, wl = self.pa, self.d, self.case.wl
+        pa.rope_kv_write(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
+                         self.cache, status=self.status)
+        if ev is not None:
+            ev[0].record()
+        pa.prefill_varlen(d["q"], self.cache, d["cuq"], d["cuk"], d["bt"], self.md["max_seqlen_q"],
+                          wl.n_kv_heads, out=self.out, status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.pinned = {k_: torch.from_numpy(np.ascontiguousarray(v_)).pin_memory()
+                       for k_, v_ in self.host.items()}
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v_.numel() * v_.element_size() for v_ in self.pinned.values())
+        return h2d, self.out_host.numel() * self.out_host.element_size()
+
+    def e2e_step(self):
+        for k_, v_ in self.pinned.items():
+            self.d[k_].copy_(v_, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def kernel_name(self):
+        return "prefill_kernel"
+
+
+def make_bench(name, dev):
+    return (PrefillBench if W.WORKLOADS[name].kind == "prefill" else DecodeBench)(name, dev)
+
+
+def rate(units, seconds, unit):
+    return units / seconds / (1e9 if unit == "GB/s" else 1e12)
+
+
+def time_bench(b, steps, warmup, dist_ctx, clocks=None):
+    """Returns dict: ms_per_step (max over ranks), kernel_ms (mean per launch)."""
+    torch = b.torch
+    for _ in range(warmup):
+        b.step()
+    torch.cuda.synchronize()
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        b.step(kev[i])
+    stop.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    ms = start.elapsed_time(stop) / steps
+    kms = sum(a.elapsed_time(z) for a, z in kev) / steps
+    st = int(b.status.item())
+    return dict(ms=dist_ctx.max(ms), kernel_ms=dist_ctx.max(kms), status=st)
+
+
+def time_e2e(b, steps, warmup, dist_ctx):
+    torch = b.torch
+    h2d, d2h = b.e2e_setup()
+    for _ in range(warmup):
+        b.e2e_step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        b.e2e_step()
+    stop.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    return dist_ctx.max(start.elapsed_time(stop) / steps), h2d, d2h
+
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_decode_seq(args):
+    name, s = args
+    from oracle import reference as orc
+    case = W.make_case(name)
+    wl = case.wl
+    blocks = [int(b) for b in case.block_tables[s] if b >= 0]
+    cache = W.initial_cache(case, blocks=blocks)
+    t0 = time.perf_counter()
+    md = orc.decode_metadata(case.num_cached[s:s + 1], case.block_tables[s:s + 1], wl.block_size)
+    q = orc.rope_pinned(case.q[s:s + 1], md["positions"], wl.head_dim, wl.rope_theta)
+    k = orc.rope_pinned(case.k[s:s + 1], md["positions"], wl.head_dim, wl.rope_theta)
+    orc.kv_write(cache, 0, k, case.v[s:s + 1], md["slot_mapping"])
+    orc.attention_decode(q, cache, 0, case.block_tables[s:s + 1], md["context_lens"],
+                         wl.n_heads, wl.n_kv_heads)
+    dt = time.perf_counter() - t0
+    return dt, (int(case.num_cached[s]) + 1) * wl.n_kv_heads * wl.head_dim * 4
+
+
+def _oracle_prefill_seq(args):
+    name, s = args
+    from oracle import reference as orc
+    case = W.make_case(name)
+    wl = case.wl
+    blocks = [int(b) for b in case.block_tables[s] if b >= 0]
+    cache = W.initial_cache(case, blocks=blocks)
+    t0 = time.perf_counter()
+    nc, nn = case.num_cached[s:s + 1], case.num_new[s:s + 1]
+    md = orc.prefill_metadata(nc, nn, case.block_tables[s:s + 1], wl.block_size)
+    lo = int(case.num_new[:s].sum())
+    hi = lo + int(nn[0])
+    q = orc.rope_pinned(case.q[lo:hi], md["positions"], wl.head_dim, wl.rope_theta)
+    k = orc.rope_pinned(case.k[lo:hi], md["positions"], wl.head_dim, wl.rope_theta)
+    orc.kv_write(cache, 0, k, case.v[lo:hi], md["slot_mapping"])
+    orc.attention_prefill(q, cache, 0, md["cu_seqlens_q"], md["cu_seqlens_k"],
+                          case.block_tables[s:s + 1], wl.n_heads, wl.n_kv_heads)
+    dt = time.perf_counter() - t0
+    p, n = int(nc[0]), int(nn[0])
+    return dt, 4 * wl.head_dim * wl.n_heads * (n * (p + 1) + n * (n - 1) // 2)
+
+
+def _single_thread_env():
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+
+
+def oracle_baseline(name, budget_s=12.0):
+    """Time the oracle on a bounded sample of the workload's sequences, one
+    sequence per worker process (single-threaded BLAS each), all host cores.
+    The clock covers only the oracle's arithmetic of each sequence (the
+    synthetic input generation is excluded)."""
+    import multiprocessing as mp
+    wl = W.WORKLOADS[name]
+    case = W.make_case(name)
+    B = len(case.num_new)
+    cores = os.cpu_count() or 1
+    fn = _oracle_prefill_seq if wl.kind == "prefill" else _oracle_decode_seq
+    # smallest sequences first would flatter nobody: take them in order
+    order = list(range(B))
+    ctx = mp.get_context("spawn")
+    t_all = time.perf_counter()
+    done, units, cpu_s = [], 0, 0.0
+    with ctx.Pool(cores, initializer=_single_thread_env) as pool:
+        pending = [pool.apply_async(fn, ((name, s),)) for s in order[:cores]]
+        nxt = cores
+        while pending:
+            r = pending.pop(0).get()
+            done.append(r)
+            cpu_s += r[0]
+            units += r[1]
+            if nxt < B and time.perf_counter() - t_all < budget_s:
+                pending.append(pool.apply_async(fn, ((name, order[nxt]),)))
+                nxt += 1
+    n = len(done)
+    # throughput of `cores` workers running side by side: units / (cpu seconds / cores)
+    wall = cpu_s / min(cores, n)
+    unit = "TFLOP/s" if wl.kind == "prefill" else "GB/s"
+    return dict(value=rate(units, wall, unit), unit=unit, cores=min(cores, n), kind="oracle",
+                sample=f"{n} of {B} sequences of {name}, one per single-threaded worker, "
+                       f"{cpu_s:.1f} CPU-s of oracle arithmetic")
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    dctx = DistCtx()
+    peaks = load_peaks()
+
+    if args.impl == "reference":
+        if dctx.rank != 0:
+            return
+        steps = args.steps or 3
+        vals = []
+        for _ in range(steps):
+            vals.append(oracle_baseline(args.workload, budget_s=8.0))
+        v = float(np.median([x["value"] for x in vals]))
+        unit = vals[0]["unit"]
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit,
+                "n_gpus": args.gpus, "steps": steps, "warmup": 0,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload},
+                "cpu_baseline": dict(vals[0], value=v),
+                "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    torch.cuda.set_device(dctx.local)
+    dev = f"cuda:{dctx.local}"
+    from paged_kv_gqa_rope_gb300 import pa
+    pa.lib()
+    wl = W.WORKLOADS[args.workload]
+    b = make_bench(args.workload, dev)
+    steps = args.steps or (4000 if wl.kind != "prefill" else 2000)
+    with ClockSampler(dctx.local) as clk:
+        r = time_bench(b, steps, warmup, dctx)
+    e2e_ms, h2d, d2h = time_e2e(b, max(10, steps // 4), warmup, dctx)
+    value = rate(b.units * dctx.world, r["ms"] / 1e3, b.unit)
+    achieved = rate(b.units, r["kernel_ms"] / 1e3, b.unit)
+    if b.unit == "GB/s":
+        peak, bound, punit, pkind = peaks[0], "hbm", "GB/s", peaks[3]
+    else:
+        peak, bound, punit, pkind = peaks[1], "tensor", "TFLOP/s", peaks[3]
+    line = {
+        "metric": METRIC, "value": value, "unit": b.unit, "n_gpus": dctx.world,
+        "steps": steps, "warmup": warmup, "ms_per_step": r["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)",
+        "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": args.workload, "n_heads": wl.n_heads,
+                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "batch": len(b.case.num_new),
+                   "l2": "inputs larger than L2 (KV cache >= 1 GB per step)",
+                   "parallelism": "replicas" if dctx.world > 1 else "single GPU"},
+        "roofline": {"bound": bound, "kernel": b.kernel_name(), "achieved": achieved,
+                     "peak": peak, "peak_source": pkind, "unit": punit,
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel_ms": r["kernel_ms"]},
+        "e2e": {"value": rate(b.units * dctx.world, e2e_ms / 1e3, b.unit), "unit": b.unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": b.launches_per_step * steps,
+        "clocks": clk.summary(),
+        "device_status": r["status"],
+    }
+    if not args.no_extra and dctx.world == 1:
+        extra = {}
+        del b
+        torch.cuda.empty_cache()
+        for name in ("gqa_decode_70b", "ragged_decode", "prefill_13b"):
+            if name == args.workload:
+                continue
+            try:
+                eb = make_bench(name, dev)
+                n = 1000 if eb.unit == "GB/s" else 400
+                er = time_bench(eb, n, warmup, dctx)
+                ach = rate(eb.units, er["kernel_ms"] / 1e3, eb.unit)
+                pk = peaks[0] if eb.unit == "GB/s" else peaks[1]
+                extra[name] = {"value": rate(eb.units, er["ms"] / 1e3, eb.unit),
+                               "unit": eb.unit, "ms_per_step": er["ms"],
+                               "kernel": eb.kernel_name(), "kernel_ms": er["kernel_ms"],
+                               "kernel_achieved": ach, "frac_of_peak": ach / pk,
+                               "steps": n, "device_status": er["status"]}
+                del eb
+                torch.cuda.empty_cache()
+            except Exception as e:  # report, keep the headline
+                extra[name] = {"error": f"{type(e).__name__}: {e}"}
+        line["per_workload"] = extra
+    if dctx.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(args.workload)
+    if dctx.rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

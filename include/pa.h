@@ -1,0 +1,238 @@
+/*
+ * pa.h - C ABI of the paged-KV GQA attention hot path for GB300 (sm_103a).
+ *
+ * The four steps of one attention layer of a Llama-2-style paged-KV engine:
+ *
+ *   pa_rope_kv_write   rotary embedding of the new tokens' Q and K at their
+ *                      true positions, and the write of their K/V into the
+ *                      block-paged cache through slot_mapping;
+ *   pa_prefill_varlen  causal attention over a flattened stream of new
+ *                      tokens (cu_seqlens_q / cu_seqlens_k), reading any
+ *                      cached prefix through block_tables;
+ *   pa_decode          attention of one new query per sequence against all
+ *                      of its cached K/V, Q heads grouped onto KV heads;
+ *   pa_alloc_cache     the block pool itself.
+ *
+ * plus host-side metadata builders (positions, cu_seqlens, slot_mapping,
+ * context_lens) and the RoPE table.
+ *
+ * Conventions for every entry point:
+ *  - Pointers documented "device" are CUDA device pointers owned by the
+ *    caller (the library never frees them); "host" pointers are plain host
+ *    memory.  All tensors are dense and row-major in the stated shape.
+ *  - fp16 is IEEE binary16 (stored as uint16_t bits); metadata is int32.
+ *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and is asynchronous: no entry point synchronises the
+ *    stream except pa_rope_table_init.
+ *  - The return value is a pa_status code.  Arguments are checked on the
+ *    host before anything is enqueued; an invalid call returns
+ *    PA_ERR_INVALID / PA_ERR_UNSUPPORTED and touches no memory.
+ *  - Device-side checks: metadata values that only exist on the device
+ *    (slots, positions, block ids, lengths) are range-checked by the
+ *    kernels.  A bad value is never dereferenced; the kernel skips the
+ *    access and ORs a PA_DEV_* bit into *dev_status (a caller-owned device
+ *    int32, may be NULL to skip reporting).  The caller reads it after the
+ *    stream has finished and clears it when it wants to.
+ *  - Nothing aborts, traps or waits without a bound; every wait inside a
+ *    kernel gives up after about a second and reports PA_DEV_TIMEOUT.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *pa_stream_t; /* cudaStream_t */
+
+/* Return codes. */
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,     /* bad shape, null pointer, misalignment, ... */
+    PA_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, block_size, group size, device */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy, malloc) */
+    PA_ERR_WORKSPACE = 4    /* the decode workspace is smaller than the call needs */
+};
+
+/* Bits that kernels OR into *dev_status. */
+enum pa_device_status {
+    PA_DEV_BAD_SLOT = 1,      /* slot_mapping entry >= num_blocks * block_size */
+    PA_DEV_BAD_POSITION = 2,  /* position < 0 or >= the RoPE table's rows */
+    PA_DEV_BAD_BLOCK = 4,     /* block_tables entry outside [0, num_blocks) */
+    PA_DEV_BAD_LENGTH = 8,    /* cu_seqlens / context_lens inconsistent or too long */
+    PA_DEV_TIMEOUT = 16,      /* a bounded wait inside a kernel gave up */
+    PA_DEV_WORKSPACE = 32     /* more decode chunks than the workspace holds */
+};
+
+/*
+ * The paged KV cache: one fp16 pool laid out as
+ *     [2 (K, V)][layers][num_blocks][block_size][n_kv_heads][head_dim]
+ * ("nano-vllm notes - Llama", allocate_kv_cache).  Physical slot
+ * `slot` of layer l is block slot / block_size, row slot % block_size.
+ */
+typedef struct {
+    void *base;           /* device pointer to element [0][0][0][0][0][0] */
+    int32_t layers;
+    int32_t num_blocks;
+    int32_t block_size;   /* tokens per block; 16 is the built size */
+    int32_t n_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t owns;         /* 1 if pa_alloc_cache allocated base */
+    int64_t layer_stride; /* elements between consecutive layers */
+    int64_t kv_stride;    /* elements between the K and the V plane */
+} pa_cache_t;
+
+/* Bytes of the pool: 2 * layers * num_blocks * block_size * n_kv_heads *
+ * head_dim * 2 (fp16).  0 for non-positive arguments. */
+size_t pa_cache_bytes(int layers, int num_blocks, int block_size, int n_kv_heads, int head_dim);
+
+/* Describe a pool.  With device_base == NULL the library cudaMallocs
+ * pa_cache_bytes(...) bytes (contents undefined) and sets owns = 1;
+ * otherwise it wraps the caller's allocation (at least that many bytes,
+ * 256-byte aligned) and sets owns = 0.  Errors: PA_ERR_INVALID (shape,
+ * alignment, out == NULL), PA_ERR_UNSUPPORTED (block_size != 16, head_dim
+ * not 64/128), PA_ERR_CUDA (allocation failed). */
+int pa_alloc_cache(pa_cache_t *out, int layers, int num_blocks, int block_size,
+                   int n_kv_heads, int head_dim, void *device_base);
+
+/* Free the pool if the library owns it; clears *cache either way. */
+int pa_free_cache(pa_cache_t *cache);
+
+/*
+ * Metadata of one prefill call ("nano-vllm notes - Llama", prepare_prefill),
+ * host to host.  For sequence s with num_cached[s] tokens already cached and
+ * num_new[s] new ones, its new tokens sit at positions
+ * num_cached[s] .. num_cached[s]+num_new[s]-1 and are written to slot
+ * block_tables[s][pos / block_size] * block_size + pos % block_size.
+ *   block_tables   host int32 [num_seqs][max_blocks_per_seq]
+ *   positions      host int32 [sum num_new]          (output)
+ *   slot_mapping   host int32 [sum num_new]          (output)
+ *   cu_seqlens_q   host int32 [num_seqs + 1]         (output)
+ *   cu_seqlens_k   host int32 [num_seqs + 1]         (output; seqlen_k = cached + new)
+ *   max_seqlen_q/k host int32 scalars               (output, may be NULL)
+ * Returns PA_ERR_INVALID for negative lengths, a block table row too short
+ * for its sequence, or a negative block id on a needed entry.
+ */
+int pa_prepare_prefill(int num_seqs, const int32_t *num_cached, const int32_t *num_new,
+                       const int32_t *block_tables, int max_blocks_per_seq, int block_size,
+                       int32_t *positions, int32_t *slot_mapping, int32_t *cu_seqlens_q,
+                       int32_t *cu_seqlens_k, int32_t *max_seqlen_q, int32_t *max_seqlen_k);
+
+/*
+ * Metadata of one decode step ("nano-vllm notes - Llama", prepare_decode),
+ * host to host: sequence s feeds one token at position num_cached[s], whose
+ * K/V goes to that position's slot; afterwards context_lens[s] =
+ * num_cached[s] + 1 (the page's example: positions [5,3], context_lens [6,4]).
+ *   positions, slot_mapping, context_lens   host int32 [num_seqs] (output)
+ */
+int pa_prepare_decode(int num_seqs, const int32_t *num_cached, const int32_t *block_tables,
+                      int max_blocks_per_seq, int block_size, int32_t *positions,
+                      int32_t *slot_mapping, int32_t *context_lens);
+
+/*
+ * RoPE table ("Meta Llama source deep-dive", 3.3 precompute_freqs_cis):
+ * rows m = 0 .. max_positions-1, columns i = 0 .. head_dim/2-1, each entry a
+ * float pair {cos, sin} of the angle m * theta^(-2i/head_dim).  The angle,
+ * cos and sin are computed in double precision on the host and each rounded
+ * once to float.  device_table must hold pa_rope_table_bytes(...) bytes
+ * (16-byte aligned).  Synchronises `stream` (the host staging buffer is
+ * freed on return).
+ */
+size_t pa_rope_table_bytes(int max_positions, int head_dim);
+int pa_rope_table_init(void *device_table, int max_positions, int head_dim, double theta,
+                       pa_stream_t stream);
+
+/*
+ * Steps a1 + a2: rotate and append ("Meta Llama source deep-dive", 3.3
+ * apply_rotary_emb and 3.5 step 2; "nano-vllm notes - Llama", slot_mapping).
+ * For every new token t (num_tokens of them):
+ *   - each adjacent pair (x_2i, x_2i+1) of every head of q[t] and k[t] is
+ *     rotated by the table entry of row positions[t]:
+ *       x' = fl32(fl32(x*c) - fl32(y*s)),  y' = fl32(fl32(x*s) + fl32(y*c)),
+ *     then rounded to nearest-even fp16 and stored back in place (V is not
+ *     rotated);
+ *   - the rotated k[t] and the unchanged v[t] are copied bit for bit to slot
+ *     slot_mapping[t] of `layer` (K plane and V plane).  slot < 0 means no
+ *     write (a padding token).
+ *   q     device fp16 [num_tokens][n_heads][head_dim], rotated in place
+ *   k     device fp16 [num_tokens][n_kv_heads][head_dim], rotated in place
+ *   v     device fp16 [num_tokens][n_kv_heads][head_dim]
+ *   positions, slot_mapping   device int32 [num_tokens]
+ *   rope_table   device, from pa_rope_table_init with max_positions rows
+ * A position outside [0, max_positions) leaves that token untouched and sets
+ * PA_DEV_BAD_POSITION; a slot past the pool sets PA_DEV_BAD_SLOT and skips
+ * the write.  num_tokens == 0 is a no-op.
+ */
+int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
+                     const int32_t *slot_mapping, int num_tokens, int n_heads, int n_kv_heads,
+                     int head_dim, const void *rope_table, int max_positions,
+                     const pa_cache_t *cache, int layer, int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * Step a3: varlen causal prefill ("Meta Llama source deep-dive", 3.5 and 3.8;
+ * "personal chatgpt 22 - llama2 generate", section 2; "nano-vllm notes -
+ * Llama", prepare_prefill / flash_attn_varlen_func).  Sequence s owns query
+ * rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 and
+ * L_k = cu_seqlens_k[s+1] - cu_seqlens_k[s] keys, the first
+ * p = L_k - L_q of them a cached prefix; query row i (absolute position
+ * p + i) of head h attends to keys 0 .. p + i of KV head h / (n_heads /
+ * n_kv_heads), all read from the cache through block_tables[s] (so the new
+ * tokens' K/V must already have been written by pa_rope_kv_write):
+ *     out = softmax(q k^T * scale) v,  scores and softmax in fp32, fp16 out.
+ *   q            device fp16 [total_q][n_heads][head_dim] (rotated)
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [num_seqs + 1]
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *   max_seqlen_q host bound on any L_q (sizes the grid; longer sequences
+ *                set PA_DEV_BAD_LENGTH and are not computed past it)
+ *   out          device fp16 [total_q][n_heads][head_dim]
+ *   scale        softmax scale; pass 0 for 1/sqrt(head_dim)
+ * Built for head_dim 64 and 128 and any n_heads divisible by n_kv_heads;
+ * Q.K^T and P.V run on the tcgen05 tensor cores with TMEM accumulators.
+ */
+int pa_prefill_varlen(const void *q, const pa_cache_t *cache, int layer,
+                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                      const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+                      int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
+                      void *out, int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * Step a4: single-token GQA decode ("personal chatgpt 22 - llama2 generate",
+ * section 3; "nano-vllm notes - Llama", prepare_decode /
+ * flash_attn_with_kvcache).  Sequence s has context_lens[s] cached tokens
+ * (its new token's K/V already appended); its query attends to all of them:
+ *     out[s][h] = softmax(q[s][h] . K^T * scale) V   over KV head h / g.
+ * The context is cut into chunks of 256 tokens spread over the GPU; each
+ * chunk's (max, sum, weighted V) is merged with the others by an online
+ * softmax in the last chunk to finish.
+ *   q             device fp16 [num_seqs][n_heads][head_dim] (rotated)
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq*block_size]
+ *   workspace     device, pa_decode_workspace_bytes(...) bytes, 256-byte
+ *                 aligned, ZEROED by the caller before its first use; every
+ *                 call leaves its counters at zero again.  One call at a time
+ *                 per workspace.
+ *   out           device fp16 [num_seqs][n_heads][head_dim]
+ * total_context bounds sum(context_lens); it sizes the workspace.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                 int64_t total_context);
+int pa_decode(const void *q, const pa_cache_t *cache, int layer, const int32_t *block_tables,
+              int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+              int n_heads, int n_kv_heads, int head_dim, float scale, void *workspace,
+              size_t workspace_bytes, void *out, int32_t *dev_status, pa_stream_t stream);
+
+/* Human-readable text of a pa_status code. */
+const char *pa_strerror(int code);
+
+/* PA_OK if the current CUDA device is an sm_103 part this library was built
+ * for, PA_ERR_UNSUPPORTED for another device, PA_ERR_CUDA if there is none. */
+int pa_check_device(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

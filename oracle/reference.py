@@ -194,10 +194,11 @@ def gather_kv(cache: np.ndarray, layer: int, table_row, n_tokens: int):
     bs = cache.shape[3]
     K = np.empty((n_tokens,) + cache.shape[4:], np.float64)
     V = np.empty_like(K)
-    for j in range(n_tokens):
-        blk = int(table_row[j // bs])
-        K[j] = cache[0, layer, blk, j % bs]
-        V[j] = cache[1, layer, blk, j % bs]
+    for lb in range((n_tokens + bs - 1) // bs):      # logical block lb
+        blk = int(table_row[lb])
+        rows = min(bs, n_tokens - lb * bs)
+        K[lb * bs:lb * bs + rows] = cache[0, layer, blk, :rows]
+        V[lb * bs:lb * bs + rows] = cache[1, layer, blk, :rows]
     return K, V
 
 

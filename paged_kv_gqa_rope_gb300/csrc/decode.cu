@@ -1,0 +1,492 @@
+// Step a4: single-token GQA decode against the paged cache
+// ("personal chatgpt 22 - llama2 generate", section 3: the new query attends
+// to the whole cached history with no mask; "nano-vllm notes - Llama",
+// prepare_decode: context_lens include the token just appended;
+// "Meta Llama source deep-dive", 3.4 repeat_kv: Q head h reads KV head h/g).
+//
+// Work decomposition.  The context of sequence s is cut into chunks of 16
+// blocks (256 tokens).  A work item is (chunk, KV head); items are spread
+// round-robin over a persistent grid of CTAs.  Each CTA holds the prefix sum
+// of chunk counts in shared memory to map an item index to its sequence.
+//
+// Inside a CTA one producer warp streams the item's K and V block tiles
+// (16 tokens x head_dim fp16 of one KV head, 4 KB each at d=128) with TMA into
+// a ring of shared-memory stages; four consumer warps take the blocks of the
+// item in turn.  Each warp computes, with warp-level tensor-core MMAs,
+//     S^T (16 tokens x 8 heads) = K (16 x d) . Q^T (d x 8 heads)
+// so the g Q heads that share the KV head form the N = 8 dimension and every
+// K/V byte is read once for the whole group; the online softmax runs on the
+// accumulator fragments with warp shuffles; P is rounded to fp16, transposed
+// in registers (movmatrix) and multiplied into
+//     O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads).
+// The four warps' (max, sum, O) are merged through shared memory.  A
+// sequence with one chunk writes its output directly; otherwise each chunk
+// stores (max, sum, O) in the workspace and the CTA that finishes the last
+// chunk of a (sequence, KV head) merges them (online-softmax reduction),
+// writes the output and resets the arrival counter to zero.
+//
+// Bound: HBM.  Algorithmic bytes per sequence = context_len * Hk * d * 2 (K
+// and V) * 2 B.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kChunkBlocks = 16;
+constexpr int kChunkTokens = kChunkBlocks * kBlockSize;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxSeqs = 4096;
+constexpr int kGroupPad = 8;  // MMA N: Q heads per KV head, padded
+
+struct DecodeArgs {
+    const __half *q;              // [B][H][D]
+    const int32_t *block_tables;  // [B][maxb]
+    const int32_t *context_lens;  // [B]
+    __half *out;                  // [B][H][D]
+    int32_t *counters;            // [B][Hk] arrival counters
+    float *part;                  // [cap][H][D + 4]: O (unnormalised), m, l
+    int32_t *status;
+    float scale_log2;             // scale * log2(e)
+    int B, H, Hk, g, maxb, num_blocks, plane_k, plane_v, cap_chunks;
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kTileBytes = kBlockSize * D * 2;  // one K or V block tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+};
+
+__device__ __forceinline__ void item_of(int w, const int *prefix, int B, int Hk, int &s, int &kvh,
+                                        int &c) {
+    const int gc = w / Hk;
+    kvh = w - gc * Hk;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= gc)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    s = lo;
+    c = gc - prefix[lo];
+}
+
+__device__ __forceinline__ int chunks_of(int ctx) { return (ctx + kChunkTokens - 1) / kChunkTokens; }
+
+// Byte offset inside a K or V block tile written by TMA with 128-byte
+// swizzle: row r (token) of the tile holds D/64 lines of 128 B; line
+// index = r * (D/64) + half; the 16-byte piece p of a line is stored at
+// position p ^ (line % 8).
+template <int D>
+__device__ __forceinline__ uint32_t tile_offset(int row, int piece16) {
+    const int half = piece16 >> 3;
+    const int line = row * (D / 64) + half;
+    return (uint32_t)(line * 128 + (((piece16 & 7) ^ (line & 7)) << 4));
+}
+
+template <int D, int NSTAGE>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeArgs a) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stages = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * L::kStageBytes);
+    uint64_t *empty = full + NSTAGE;
+    int *stage_bad = reinterpret_cast<int *>(empty + NSTAGE);
+    float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
+    float *sm_m = sm_o + kConsumerWarps * kGroupPad * D;           // [4][8]
+    float *sm_l = sm_m + kConsumerWarps * kGroupPad;               // [4][8]
+    int *sm_flag = reinterpret_cast<int *>(sm_l + kConsumerWarps * kGroupPad);
+    int *prefix = sm_flag + 4;                                     // [B + 1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B;
+
+    // -------- chunk counts and their prefix sum (every CTA, in smem)
+    for (int s = tid; s < B; s += kThreads) {
+        const int ctx = __ldg(a.context_lens + s);
+        int n = 0;
+        if (ctx >= 1 && ctx <= a.maxb * kBlockSize)
+            n = chunks_of(ctx);
+        else if (blockIdx.x == 0)
+            report(a.status, PA_DEV_BAD_LENGTH);
+        prefix[s + 1] = n;
+    }
+    if (tid < NSTAGE) stage_bad[tid] = 0;
+    if (tid == 0) {
+        prefix[0] = 0;
+        sm_flag[0] = sm_flag[1] = 0;
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {  // inclusive scan of prefix[1..B] by one warp
+        int carry = 0;
+        for (int base = 1; base <= B; base += 32) {
+            const int i = base + lane;
+            int v = i <= B ? prefix[i] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (i <= B) prefix[i] = v + carry;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+    const int total_chunks = prefix[B];
+    if (total_chunks > a.cap_chunks) {
+        if (blockIdx.x == 0 && tid == 0) report(a.status, PA_DEV_WORKSPACE);
+        return;
+    }
+    const int total_items = total_chunks * a.Hk;
+
+    if (warp == kConsumerWarps) {
+        // ================= producer warp: TMA block tiles into the ring
+        if (lane == 0) tma_prefetch_desc(&kvmap);
+        int gblk = 0;
+        bool abort = false;
+        for (int w = blockIdx.x; w < total_items && !abort; w += gridDim.x) {
+            int s, kvh, c;
+            item_of(w, prefix, B, a.Hk, s, kvh, c);
+            const int ctx = __ldg(a.context_lens + s);
+            const int nblk_seq = (ctx + kBlockSize - 1) / kBlockSize;
+            const int b0 = c * kChunkBlocks;
+            const int nb = min(kChunkBlocks, nblk_seq - b0);
+            const int my_blk =
+                lane < nb ? __ldg(a.block_tables + (int64_t)s * a.maxb + b0 + lane) : 0;
+            for (int j = 0; j < nb; ++j) {
+                const int blk = __shfl_sync(0xffffffffu, my_blk, j);
+                const int stage = gblk % NSTAGE;
+                const uint32_t ph = (gblk / NSTAGE) & 1;
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(&empty[stage], ph ^ 1);
+                    if (!ok) {
+                        report(a.status, PA_DEV_TIMEOUT);
+                    } else if (blk >= 0 && blk < a.num_blocks) {
+                        uint8_t *dst = stages + stage * L::kStageBytes;
+                        mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                        tma_load_5d(dst, &kvmap, &full[stage], 0, 0, kvh, blk * kBlockSize,
+                                    a.plane_k);
+                        tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0, kvh,
+                                    blk * kBlockSize, a.plane_v);
+                    } else {
+                        report(a.status, PA_DEV_BAD_BLOCK);
+                        stage_bad[stage] = 1;
+                        mbar_arrive(&full[stage]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    abort = true;
+                    break;
+                }
+                ++gblk;
+            }
+        }
+        // Leave no copy in flight: wait (bounded) for the last stages issued.
+        if (lane == 0) {
+            for (int i = max(0, gblk - NSTAGE); i < gblk; ++i)
+                mbar_wait(&full[i % NSTAGE], (i / NSTAGE) & 1);
+        }
+        return;
+    }
+
+    // ===================== consumer warps
+    const int head = lane >> 2;          // B-operand column (Q head in group)
+    const int quad = lane & 3;
+    const int h0 = 2 * quad;             // accumulator columns held by this lane
+    int gblk = 0;
+    for (int w = blockIdx.x; w < total_items; w += gridDim.x) {
+        int s, kvh, c;
+        item_of(w, prefix, B, a.Hk, s, kvh, c);
+        const int ctx = __ldg(a.context_lens + s);
+        const int nblk_seq = (ctx + kBlockSize - 1) / kBlockSize;
+        const int b0 = c * kChunkBlocks;
+        const int nb = min(kChunkBlocks, nblk_seq - b0);
+        const int n_chunks = chunks_of(ctx);
+
+        // Q^T fragments (B operand): Q[head][16kk + 2*quad + {0,1}] and +8.
+        uint32_t qb[D / 16][2];
+        {
+            const bool hv = head < a.g;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                a.q + ((int64_t)s * a.H + kvh * a.g + (hv ? head : 0)) * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qb[kk][0] = hv ? __ldg(qrow + kk * 8 + quad) : 0u;
+                qb[kk][1] = hv ? __ldg(qrow + kk * 8 + 4 + quad) : 0u;
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float o[D / 16][4];
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+        bool abort = false;
+        for (int j = warp; j < nb; j += kConsumerWarps) {
+            const int gb = gblk + j;
+            const int stage = gb % NSTAGE;
+            if (!mbar_wait(&full[stage], (gb / NSTAGE) & 1)) {
+                if (lane == 0) report(a.status, PA_DEV_TIMEOUT);
+                abort = true;
+                break;
+            }
+            const int bad = stage_bad[stage];
+            if (!bad) {
+                const uint32_t kt = smem_u32(stages + stage * L::kStageBytes);
+                const uint32_t vt = kt + L::kTileBytes;
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t af[4];
+                    ldmatrix_x4(af, kt + tile_offset<D>(krow, kk * 2 + (lane >> 4)));
+                    mma_16816(sc, af, qb[kk][0], qb[kk][1]);
+                }
+                const int tok = (b0 + j) * kBlockSize + (lane >> 2);
+                float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
+                float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+                if (tok >= ctx) x0 = x1 = -INFINITY;
+                if (tok + 8 >= ctx) x2 = x3 = -INFINITY;
+                float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                const __half2 p01 = __floats2half2_rn(ex2(x0 - mn0), ex2(x1 - mn1));
+                const __half2 p23 = __floats2half2_rn(ex2(x2 - mn0), ex2(x3 - mn1));
+                l0 = l0 * al0 + __low2float(p01) + __low2float(p23);
+                l1 = l1 * al1 + __high2float(p01) + __high2float(p23);
+                const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
+                const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
+                const int vrow = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                    uint32_t af[4];
+                    ldmatrix_x4_trans(af, vt + tile_offset<D>(vrow, mt * 2 + ((lane >> 3) & 1)));
+                    mma_16816(o[mt], af, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (bad) stage_bad[stage] = 0;
+                mbar_arrive(&empty[stage]);
+            }
+        }
+        // A timed-out wait leaves the ring out of step: every consumer warp
+        // learns of it at the barrier below and the CTA stops after this item.
+        if (__any_sync(0xffffffffu, abort) && lane == 0) atomicOr(sm_flag + 1, 1);
+        gblk += nb;
+
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        if (lane < 4) {
+            sm_m[warp * kGroupPad + h0] = m0;
+            sm_m[warp * kGroupPad + h0 + 1] = m1;
+            sm_l[warp * kGroupPad + h0] = l0;
+            sm_l[warp * kGroupPad + h0 + 1] = l1;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            float *ow = sm_o + (warp * kGroupPad + h0) * D;
+            ow[d] = o[mt][0];
+            ow[D + d] = o[mt][1];
+            ow[d + 8] = o[mt][2];
+            ow[D + d + 8] = o[mt][3];
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);
+        abort = sm_flag[1] != 0;
+
+        const int gc = prefix[s] + c;
+        for (int idx = tid; idx < a.g * D; idx += kConsumerWarps * 32) {
+            const int h = idx / D, d = idx - (idx / D) * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int wv = 0; wv < kConsumerWarps; ++wv) M = fmaxf(M, sm_m[wv * kGroupPad + h]);
+            float O = 0.f, Lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int wv = 0; wv < kConsumerWarps; ++wv) {
+                    const float f = ex2(sm_m[wv * kGroupPad + h] - M);
+                    Lsum += f * sm_l[wv * kGroupPad + h];
+                    O += f * sm_o[(wv * kGroupPad + h) * D + d];
+                }
+            }
+            const int hq = kvh * a.g + h;
+            if (n_chunks == 1) {
+                a.out[((int64_t)s * a.H + hq) * D + d] = __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
+            } else {
+                float *rec = a.part + ((int64_t)gc * a.H + hq) * (D + 4);
+                rec[d] = O;
+                if (d == 0) {
+                    rec[D] = M;
+                    rec[D + 1] = Lsum;
+                }
+            }
+        }
+        if (n_chunks > 1) {
+            __threadfence();
+            named_barrier_sync(1, kConsumerWarps * 32);
+            if (tid == 0) {
+                const int prev = atomicAdd(a.counters + s * a.Hk + kvh, 1);
+                *sm_flag = (prev == n_chunks - 1);
+            }
+            named_barrier_sync(1, kConsumerWarps * 32);
+            if (*sm_flag) {
+                __threadfence();
+                const int gc0 = prefix[s];
+                for (int idx = tid; idx < a.g * D; idx += kConsumerWarps * 32) {
+                    const int h = idx / D, d = idx - (idx / D) * D;
+                    const int hq = kvh * a.g + h;
+                    const float *rec0 = a.part + ((int64_t)gc0 * a.H + hq) * (D + 4);
+                    const int64_t stride = (int64_t)a.H * (D + 4);
+                    float M = -INFINITY;
+                    for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(rec0 + cc * stride + D));
+                    float O = 0.f, Lsum = 0.f;
+                    if (M != -INFINITY) {
+                        for (int cc = 0; cc < n_chunks; ++cc) {
+                            const float *rec = rec0 + cc * stride;
+                            const float f = ex2(__ldcg(rec + D) - M);
+                            Lsum += f * __ldcg(rec + D + 1);
+                            O += f * __ldcg(rec + d);
+                        }
+                    }
+                    a.out[((int64_t)s * a.H + hq) * D + d] =
+                        __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
+                }
+                if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
+            }
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);  // smem merge area free again
+        if (abort) break;
+    }
+}
+
+template <int D, int NSTAGE>
+size_t decode_smem_bytes(int B) {
+    return 1024 + (size_t)NSTAGE * Layout<D>::kStageBytes + 2 * NSTAGE * sizeof(uint64_t) +
+           NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
+           4 * sizeof(int) + (size_t)(B + 1) * sizeof(int);
+}
+
+constexpr int kStages = 8;
+
+template <int D>
+int launch_decode(const CUtensorMap &map, const DecodeArgs &a, cudaStream_t st) {
+    const size_t smem = decode_smem_bytes<D, kStages>(a.B);
+    // The dynamic shared-memory limit and the occupancy depend only on the
+    // device; both are set up once per device, on its first call.
+    static std::mutex mu;
+    static int per_sm_of[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    int per_sm;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (per_sm_of[dev] == 0) {
+            const size_t smax = decode_smem_bytes<D, kStages>(kMaxSeqs);
+            int n = 0;
+            if (cudaFuncSetAttribute(decode_kernel<D, kStages>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smax) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, kStages>,
+                                                              kThreads, smax) != cudaSuccess ||
+                n < 1) {
+                cudaGetLastError();
+                return PA_ERR_CUDA;
+            }
+            per_sm_of[dev] = n;
+        }
+        per_sm = per_sm_of[dev];
+    }
+    const int grid = sm_count() * per_sm;
+    decode_kernel<D, kStages><<<grid, kThreads, smem, st>>>(map, a);
+    return launch_status();
+}
+
+size_t counters_bytes(int B, int Hk) { return ((size_t)B * Hk * sizeof(int32_t) + 255) & ~(size_t)255; }
+size_t chunk_record_bytes(int H, int D) { return (size_t)H * (D + 4) * sizeof(float); }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
+                                            int head_dim, int64_t total_context) {
+    if (num_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || total_context < 0)
+        return 0;
+    const int64_t cap = num_seqs + (total_context + kChunkTokens - 1) / kChunkTokens;
+    return counters_bytes(num_seqs, n_kv_heads) + (size_t)cap * chunk_record_bytes(n_heads, head_dim);
+}
+
+extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                         int head_dim, float scale, void *workspace, size_t workspace_bytes,
+                         void *out, int32_t *dev_status, pa_stream_t stream) {
+    if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
+        max_blocks_per_seq <= 0 || !(scale >= 0.f))
+        return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (n_heads / n_kv_heads > kGroupPad || num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+    if (!cache_ok(cache, layer, n_kv_heads, head_dim)) return PA_ERR_INVALID;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out || !workspace) return PA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_INVALID;
+    const size_t cnt = counters_bytes(num_seqs, n_kv_heads);
+    if (workspace_bytes < cnt + chunk_record_bytes(n_heads, head_dim)) return PA_ERR_WORKSPACE;
+    const int64_t cap = (workspace_bytes - cnt) / chunk_record_bytes(n_heads, head_dim);
+
+    CUtensorMap map;
+    if (!make_cache_map(&map, cache, head_dim / 64, kBlockSize)) return PA_ERR_CUDA;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)head_dim);
+
+    DecodeArgs a;
+    a.q = static_cast<const __half *>(q);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = static_cast<__half *>(out);
+    a.counters = static_cast<int32_t *>(workspace);
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cnt);
+    a.status = dev_status;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.B = num_seqs;
+    a.H = n_heads;
+    a.Hk = n_kv_heads;
+    a.g = n_heads / n_kv_heads;
+    a.maxb = max_blocks_per_seq;
+    a.num_blocks = cache->num_blocks;
+    a.plane_k = layer;
+    a.plane_v = cache->layers + layer;
+    a.cap_chunks = (int)(cap > INT32_MAX ? INT32_MAX : cap);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return head_dim == 128 ? launch_decode<128>(map, a, st) : launch_decode<64>(map, a, st);
+}

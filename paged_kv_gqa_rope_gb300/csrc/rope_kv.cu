@@ -1,0 +1,140 @@
+// Steps a1 + a2: rotary embedding of the new tokens' Q/K in place and the
+// append of their K/V to the paged cache through slot_mapping
+// ("Meta Llama source deep-dive", 3.3 apply_rotary_emb and 3.5 step 2;
+// "nano-vllm notes - Llama", slot_mapping).
+//
+// One thread moves one 16-byte piece (8 fp16 = 4 rotation pairs) of one head
+// row.  A token has n_heads Q rows, n_kv_heads K rows and n_kv_heads V rows;
+// consecutive threads take consecutive pieces, so every warp reads and writes
+// whole 128-byte lines.  The kernel is bound by HBM: it reads Q, K and V once
+// and writes Q, K, cache K and cache V once.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+struct RopeArgs {
+    __half *q;
+    __half *k;
+    const __half *v;
+    const int32_t *positions;
+    const int32_t *slots;
+    const float2 *table;  // [max_pos][d/2] {cos, sin}
+    __half *kcache;       // K plane of the layer: [num_slots][Hk][d]
+    __half *vcache;
+    int64_t num_slots;
+    int32_t *status;
+    int num_tokens, n_heads, n_kv_heads, max_pos;
+};
+
+// Rotate 4 pairs with the pinned fp32 arithmetic: no contraction into FMA,
+// each product and sum rounded to fp32, the result rounded to nearest-even
+// fp16.
+__device__ __forceinline__ uint4 rotate8(uint4 x, const float4 cs01, const float4 cs23) {
+    const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
+    const float s[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w[i]);
+        const float a = __low2float(h), b = __high2float(h);
+        const float re = __fsub_rn(__fmul_rn(a, c[i]), __fmul_rn(b, s[i]));
+        const float im = __fadd_rn(__fmul_rn(a, s[i]), __fmul_rn(b, c[i]));
+        __half2 r = __halves2half2(__float2half_rn(re), __float2half_rn(im));
+        w[i] = *reinterpret_cast<uint32_t *>(&r);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
+    constexpr int kPieces = D / 8;  // 16-byte pieces per head row
+    const int rows = a.n_heads + 2 * a.n_kv_heads;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = (int64_t)a.num_tokens * rows * kPieces;
+    if (idx >= total) return;
+    const int piece = (int)(idx % kPieces);
+    const int row = (int)((idx / kPieces) % rows);
+    const int t = (int)(idx / ((int64_t)kPieces * rows));
+
+    const int pos = __ldg(a.positions + t);
+    if (pos < 0 || pos >= a.max_pos) {
+        if (row == 0 && piece == 0) report(a.status, PA_DEV_BAD_POSITION);
+        return;
+    }
+    const int slot = __ldg(a.slots + t);
+    const bool write_cache = slot >= 0 && slot < a.num_slots;
+    if (slot >= a.num_slots && row == 0 && piece == 0) report(a.status, PA_DEV_BAD_SLOT);
+
+    const int Hk = a.n_kv_heads;
+    if (row < a.n_heads + Hk) {
+        // Q or K row: rotate in place (and append K).
+        const bool is_q = row < a.n_heads;
+        __half *base = is_q ? a.q + ((int64_t)t * a.n_heads + row) * D
+                            : a.k + ((int64_t)t * Hk + (row - a.n_heads)) * D;
+        uint4 *p = reinterpret_cast<uint4 *>(base) + piece;
+        const float4 *cs = reinterpret_cast<const float4 *>(a.table + (int64_t)pos * (D / 2) +
+                                                            piece * 4);
+        const uint4 r = rotate8(*p, __ldg(cs), __ldg(cs + 1));
+        *p = r;
+        if (!is_q && write_cache) {
+            const int h = row - a.n_heads;
+            reinterpret_cast<uint4 *>(a.kcache + ((int64_t)slot * Hk + h) * D)[piece] = r;
+        }
+    } else if (write_cache) {
+        const int h = row - a.n_heads - Hk;
+        const uint4 x =
+            __ldg(reinterpret_cast<const uint4 *>(a.v + ((int64_t)t * Hk + h) * D) + piece);
+        reinterpret_cast<uint4 *>(a.vcache + ((int64_t)slot * Hk + h) * D)[piece] = x;
+    }
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
+                                const int32_t *slot_mapping, int num_tokens, int n_heads,
+                                int n_kv_heads, int head_dim, const void *rope_table,
+                                int max_positions, const pa_cache_t *cache, int layer,
+                                int32_t *dev_status, pa_stream_t stream) {
+    if (num_tokens < 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
+        max_positions <= 0)
+        return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!cache_ok(cache, layer, n_kv_heads, head_dim)) return PA_ERR_INVALID;
+    if (num_tokens == 0) return PA_OK;
+    if (!q || !k || !v || !positions || !slot_mapping || !rope_table) return PA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_table))
+        return PA_ERR_INVALID;
+    if ((int64_t)num_tokens * (n_heads + 2 * n_kv_heads) * (head_dim / 8) > (int64_t)1 << 40)
+        return PA_ERR_INVALID;
+
+    RopeArgs a;
+    a.q = static_cast<__half *>(q);
+    a.k = static_cast<__half *>(k);
+    a.v = static_cast<const __half *>(v);
+    a.positions = positions;
+    a.slots = slot_mapping;
+    a.table = static_cast<const float2 *>(rope_table);
+    a.kcache = cache_plane(cache, 0, layer);
+    a.vcache = cache_plane(cache, 1, layer);
+    a.num_slots = (int64_t)cache->num_blocks * cache->block_size;
+    a.status = dev_status;
+    a.num_tokens = num_tokens;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.max_pos = max_positions;
+
+    const int64_t total = (int64_t)num_tokens * (n_heads + 2 * n_kv_heads) * (head_dim / 8);
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128)
+        rope_kv_write_kernel<128><<<(unsigned)blocks, threads, 0, st>>>(a);
+    else
+        rope_kv_write_kernel<64><<<(unsigned)blocks, threads, 0, st>>>(a);
+    return launch_status();
+}

@@ -1,0 +1,246 @@
+"""Thin ctypes binding of libpa (include/pa.h): the same entry points, with
+torch tensors in and out.  It only checks dtypes/devices and marshals
+pointers; every step of the computation runs in the library's kernels.  If
+libpa.so has not been built, every call raises (there is no fallback).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+PA_DEV_BAD_SLOT, PA_DEV_BAD_POSITION, PA_DEV_BAD_BLOCK = 1, 2, 4
+PA_DEV_BAD_LENGTH, PA_DEV_TIMEOUT, PA_DEV_WORKSPACE = 8, 16, 32
+
+# every symbol include/pa.h declares
+EXPORTS = (
+    "pa_cache_bytes", "pa_alloc_cache", "pa_free_cache", "pa_prepare_prefill",
+    "pa_prepare_decode", "pa_rope_table_bytes", "pa_rope_table_init", "pa_rope_kv_write",
+    "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
+    "pa_check_device",
+)
+
+
+class PaCache(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("layers", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("owns", ctypes.c_int32), ("layer_stride", ctypes.c_int64),
+                ("kv_stride", ctypes.c_int64)]
+
+
+class PAError(RuntimeError):
+    def __init__(self, name, code):
+        super().__init__(f"{name} failed: {strerror(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_SIGS = {
+    "pa_cache_bytes": (_sz, [_i32] * 5),
+    "pa_alloc_cache": (_i32, [ctypes.POINTER(PaCache)] + [_i32] * 5 + [_vp]),
+    "pa_free_cache": (_i32, [ctypes.POINTER(PaCache)]),
+    "pa_prepare_prefill": (_i32, [_i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "pa_prepare_decode": (_i32, [_i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "pa_rope_table_bytes": (_sz, [_i32, _i32]),
+    "pa_rope_table_init": (_i32, [_vp, _i32, _i32, ctypes.c_double, _vp]),
+    "pa_rope_kv_write": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32,
+                                ctypes.POINTER(PaCache), _i32, _vp, _vp]),
+    "pa_prefill_varlen": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _vp, _vp, _i32, _i32,
+                                 _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
+    "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64]),
+    "pa_decode": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32, _i32,
+                         _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
+    "pa_strerror": (ctypes.c_char_p, [_i32]),
+    "pa_check_device": (_i32, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_gqa_rope_gb300.build`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().pa_strerror(int(code)).decode()
+
+
+def _check(name, rc):
+    if rc != PA_OK:
+        raise PAError(name, rc)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def check_device() -> int:
+    return lib().pa_check_device()
+
+
+# ------------------------------------------------------------------ host metadata
+
+def prepare_prefill(num_cached, num_new, block_tables, block_size=16):
+    nc = np.ascontiguousarray(num_cached, np.int32)
+    nn = np.ascontiguousarray(num_new, np.int32)
+    bt = np.ascontiguousarray(block_tables, np.int32)
+    B = len(nn)
+    T = int(nn.sum())
+    pos = np.empty(max(T, 1), np.int32)
+    slots = np.empty(max(T, 1), np.int32)
+    cuq = np.empty(B + 1, np.int32)
+    cuk = np.empty(B + 1, np.int32)
+    mq, mk = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("pa_prepare_prefill", lib().pa_prepare_prefill(
+        B, _p(nc), _p(nn), _p(bt), bt.shape[1] if bt.ndim == 2 else 0, block_size, _p(pos),
+        _p(slots), _p(cuq), _p(cuk), ctypes.byref(mq), ctypes.byref(mk)))
+    return dict(positions=pos[:T], slot_mapping=slots[:T], cu_seqlens_q=cuq, cu_seqlens_k=cuk,
+                max_seqlen_q=mq.value, max_seqlen_k=mk.value)
+
+
+def prepare_decode(num_cached, block_tables, block_size=16):
+    nc = np.ascontiguousarray(num_cached, np.int32)
+    bt = np.ascontiguousarray(block_tables, np.int32)
+    B = len(nc)
+    pos, slots, ctx = (np.empty(max(B, 1), np.int32) for _ in range(3))
+    _check("pa_prepare_decode", lib().pa_prepare_decode(
+        B, _p(nc), _p(bt), bt.shape[1], block_size, _p(pos), _p(slots), _p(ctx)))
+    return dict(positions=pos[:B], slot_mapping=slots[:B], context_lens=ctx[:B])
+
+
+# ------------------------------------------------------------------ cache and table
+
+class Cache:
+    """The block pool [2, layers, num_blocks, block_size, n_kv_heads, head_dim]
+    fp16.  By default the memory is a torch tensor (``self.tensor``) that the
+    library wraps; ``library_owned=True`` lets pa_alloc_cache allocate it."""
+
+    def __init__(self, layers, num_blocks, n_kv_heads, head_dim, block_size=16, device="cuda",
+                 library_owned=False):
+        self.desc = PaCache()
+        self.tensor = None
+        if library_owned:
+            base = None
+        else:
+            self.tensor = torch.empty((2, layers, num_blocks, block_size, n_kv_heads, head_dim),
+                                      dtype=torch.float16, device=device)
+            base = _p(self.tensor)
+        _check("pa_alloc_cache", lib().pa_alloc_cache(
+            ctypes.byref(self.desc), layers, num_blocks, block_size, n_kv_heads, head_dim, base))
+
+    def free(self):
+        if self.desc.base:
+            _check("pa_free_cache", lib().pa_free_cache(ctypes.byref(self.desc)))
+        self.tensor = None
+
+    def __del__(self):
+        try:
+            if self.desc.owns and self.desc.base:
+                lib().pa_free_cache(ctypes.byref(self.desc))
+        except Exception:
+            pass
+
+
+def cache_bytes(layers, num_blocks, block_size, n_kv_heads, head_dim) -> int:
+    return lib().pa_cache_bytes(layers, num_blocks, block_size, n_kv_heads, head_dim)
+
+
+def rope_table(max_positions, head_dim, theta=10000.0, device="cuda", stream=None):
+    nbytes = lib().pa_rope_table_bytes(max_positions, head_dim)
+    if nbytes == 0:
+        raise ValueError("bad RoPE table shape")
+    t = torch.empty((max_positions, head_dim // 2, 2), dtype=torch.float32, device=device)
+    _check("pa_rope_table_init", lib().pa_rope_table_init(
+        _p(t), max_positions, head_dim, float(theta), _stream(stream)))
+    return t
+
+
+def new_status(device="cuda"):
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ------------------------------------------------------------------ the hot path
+
+def rope_kv_write(q, k, v, positions, slot_mapping, table, cache: Cache, layer=0, status=None,
+                  stream=None):
+    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
+    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
+    _dev(table, torch.float32, "table")
+    T, H, d = q.shape
+    Hk = k.shape[1]
+    _check("pa_rope_kv_write", lib().pa_rope_kv_write(
+        _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), T, H, Hk, d, _p(table),
+        table.shape[0], ctypes.byref(cache.desc), layer, _p(status), _stream(stream)))
+
+
+def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_seqlen_q,
+                   n_kv_heads, layer=0, scale=0.0, out=None, status=None, stream=None):
+    _dev(q, torch.float16, "q"); _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _dev(cu_seqlens_k, torch.int32, "cu_seqlens_k"); _dev(block_tables, torch.int32, "block_tables")
+    T, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_prefill_varlen", lib().pa_prefill_varlen(
+        _p(q), ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
+        _p(block_tables), block_tables.shape[1], cu_seqlens_q.shape[0] - 1, int(max_seqlen_q), H,
+        n_kv_heads, d, float(scale), _p(out), _p(status), _stream(stream)))
+    return out
+
+
+def decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim, total_context) -> int:
+    return lib().pa_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim,
+                                           int(total_context))
+
+
+def decode_workspace(num_seqs, n_heads, n_kv_heads, head_dim, total_context, device="cuda"):
+    """A zeroed workspace for pa_decode (its counters must start at zero)."""
+    n = decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim, total_context)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode(q, cache: Cache, block_tables, context_lens, workspace, n_kv_heads, layer=0, scale=0.0,
+           out=None, status=None, stream=None):
+    _dev(q, torch.float16, "q"); _dev(block_tables, torch.int32, "block_tables")
+    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
+    B, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode", lib().pa_decode(
+        _p(q), ctypes.byref(cache.desc), layer, _p(block_tables), block_tables.shape[1],
+        _p(context_lens), B, H, n_kv_heads, d, float(scale), _p(workspace), workspace.numel(),
+        _p(out), _p(status), _stream(stream)))
+    return out

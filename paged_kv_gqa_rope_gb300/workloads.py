@@ -29,6 +29,7 @@ Normal distributions N(mu, s) take s as the standard deviation.  Seeds are
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -194,9 +195,12 @@ def block_contents(wl: Workload, block: int) -> np.ndarray:
     if wl.kv_std != 1.0:
         x *= np.float32(wl.kv_std)
     if wl.outlier_frac > 0.0:
-        hit = rng.random(shape) < wl.outlier_frac
-        big = rng.standard_normal(shape, dtype=np.float32) * np.float32(wl.outlier_std)
-        x = np.where(hit, big, x)
+        # outliers: a binomial count of entries (indices drawn with
+        # replacement) replaced by N(0, outlier_std)
+        flat = x.reshape(-1)
+        n_out = int(rng.binomial(flat.size, wl.outlier_frac))
+        idx = rng.integers(0, flat.size, size=n_out)
+        flat[idx] = rng.standard_normal(n_out, dtype=np.float32) * np.float32(wl.outlier_std)
     return x.astype(np.float16)
 
 
@@ -207,7 +211,19 @@ def initial_cache(case: Case, blocks=None) -> np.ndarray:
     wl = case.wl
     cache = np.zeros((2, 1, case.num_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim),
                      np.float16)
-    it = range(case.num_blocks) if blocks is None else sorted(set(int(b) for b in blocks))
-    for b in it:
-        cache[:, 0, b] = block_contents(wl, b)
+    todo = list(range(case.num_blocks)) if blocks is None else sorted(set(int(b) for b in blocks))
+
+    def fill(lo_hi):
+        for b in todo[lo_hi[0]:lo_hi[1]]:
+            cache[:, 0, b] = block_contents(wl, b)
+
+    step = 512
+    spans = [(i, min(i + step, len(todo))) for i in range(0, len(todo), step)]
+    if len(spans) > 1:
+        import concurrent.futures as cf
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, spans))
+    else:
+        for sp in spans:
+            fill(sp)
     return cache

@@ -1,0 +1,110 @@
+"""Host side of the C ABI, no GPU needed: the library loads and exports every
+symbol include/pa.h declares; the metadata builders agree bit for bit with
+the oracle; invalid arguments are rejected before anything is enqueued."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import reference as orc
+from paged_kv_gqa_rope_gb300 import pa
+from paged_kv_gqa_rope_gb300 import workloads as W
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(libpa):
+    names = declared_functions()
+    assert len(names) >= 12
+    assert set(names) == set(pa.EXPORTS)
+    for n in names:
+        assert hasattr(libpa, n), n
+
+
+def test_sizes(libpa):
+    assert pa.cache_bytes(1, 16, 16, 2, 64) == 2 * 16 * 16 * 2 * 64 * 2
+    assert pa.cache_bytes(0, 16, 16, 2, 64) == 0
+    assert libpa.pa_rope_table_bytes(100, 128) == 100 * 64 * 8
+    assert libpa.pa_rope_table_bytes(100, 7) == 0
+    assert libpa.pa_decode_workspace_bytes(32, 64, 8, 128, 32 * 4097) > 0
+    assert libpa.pa_decode_workspace_bytes(0, 64, 8, 128, 10) == 0
+
+
+def test_cache_descriptor_wraps_caller_memory(libpa):
+    d = pa.PaCache()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced on the host
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 3, 10, 16, 8, 128, fake) == pa.PA_OK
+    assert d.owns == 0 and d.layer_stride == 10 * 16 * 8 * 128 and d.kv_stride == 3 * d.layer_stride
+    assert libpa.pa_free_cache(ctypes.byref(d)) == pa.PA_OK and not d.base
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 8, 8, 128, fake) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 8, 96, fake) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 8, 128, ctypes.c_void_p(1 << 20 | 16)) == pa.PA_ERR_INVALID
+    assert libpa.pa_alloc_cache(None, 1, 10, 16, 8, 128, fake) == pa.PA_ERR_INVALID
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 0, 10, 16, 8, 128, fake) == pa.PA_ERR_INVALID
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_13b"])
+def test_prepare_prefill_matches_oracle(libpa, name):
+    c = W.make_case(name)
+    got = pa.prepare_prefill(c.num_cached, c.num_new, c.block_tables)
+    want = orc.prefill_metadata(c.num_cached, c.num_new, c.block_tables, 16)
+    for key in ("positions", "slot_mapping", "cu_seqlens_q", "cu_seqlens_k"):
+        assert np.array_equal(got[key], want[key]), key
+    assert got["max_seqlen_q"] == want["max_seqlen_q"]
+    assert got["max_seqlen_k"] == want["max_seqlen_k"]
+
+
+@pytest.mark.parametrize("name", ["mha_decode_7b", "gqa_decode_70b", "ragged_decode"])
+def test_prepare_decode_matches_oracle(libpa, name):
+    c = W.make_case(name)
+    got = pa.prepare_decode(c.num_cached, c.block_tables)
+    want = orc.decode_metadata(c.num_cached, c.block_tables, 16)
+    for key in ("positions", "slot_mapping", "context_lens"):
+        assert np.array_equal(got[key], want[key]), key
+
+
+def test_prepare_rejects_bad_metadata(libpa):
+    bt = np.array([[3, -1]], np.int32)
+    with pytest.raises(pa.PAError):
+        pa.prepare_prefill([10], [10], bt)        # needs logical block 1 (-1)
+    with pytest.raises(pa.PAError):
+        pa.prepare_prefill([0], [33], bt)         # table row too short
+    with pytest.raises(pa.PAError):
+        pa.prepare_prefill([-1], [3], bt)
+    with pytest.raises(pa.PAError):
+        pa.prepare_decode([16], bt)               # position 16 -> block 1 = -1
+    md = pa.prepare_prefill([0, 4], [0, 3], np.array([[1, -1], [2, -1]], np.int32))
+    assert md["cu_seqlens_q"].tolist() == [0, 0, 3] and md["cu_seqlens_k"].tolist() == [0, 0, 7]
+
+
+def test_kernel_entry_points_validate_before_launch(libpa):
+    d = pa.PaCache()
+    fake = ctypes.c_void_p(1 << 20)
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 2, 64, fake) == pa.PA_OK
+    buf = ctypes.c_void_p(1 << 24)
+    # head_dim 96 unsupported; H % Hk != 0 invalid; wrong cache head count invalid
+    assert libpa.pa_rope_kv_write(buf, buf, buf, buf, buf, 4, 4, 2, 96, buf, 8, ctypes.byref(d), 0, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_rope_kv_write(buf, buf, buf, buf, buf, 4, 5, 2, 64, buf, 8, ctypes.byref(d), 0, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_rope_kv_write(buf, buf, buf, buf, buf, 4, 4, 4, 64, buf, 8, ctypes.byref(d), 0, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_rope_kv_write(buf, buf, buf, buf, buf, 4, 4, 2, 64, buf, 8, ctypes.byref(d), 1, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_rope_kv_write(None, buf, buf, buf, buf, 4, 4, 2, 64, buf, 8, ctypes.byref(d), 0, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_rope_kv_write(ctypes.c_void_p((1 << 24) + 2), buf, buf, buf, buf, 4, 4, 2, 64, buf, 8, ctypes.byref(d), 0, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_rope_kv_write(None, None, None, None, None, 0, 4, 2, 64, None, 8, ctypes.byref(d), 0, None, None) == pa.PA_OK
+    # decode: group of 16 unsupported; too-small workspace; zero sequences is a no-op
+    assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 2, 32, 2, 64, 0.0, buf, 1 << 20, buf, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 2, 4, 2, 64, 0.0, buf, 16, buf, None, None) == pa.PA_ERR_WORKSPACE
+    assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 0, 4, 2, 64, 0.0, buf, 16, buf, None, None) == pa.PA_OK
+    assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 2, 4, 2, 64, -1.0, buf, 1 << 20, buf, None, None) == pa.PA_ERR_INVALID
+    # prefill: H % Hk, head_dim
+    assert libpa.pa_prefill_varlen(buf, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 5, 2, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_prefill_varlen(buf, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 96, 0.0, buf, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_strerror(pa.PA_ERR_WORKSPACE) == b"decode workspace too small"
