@@ -161,7 +161,7 @@ class DecodeBench:
                          slots=md["slot_mapping"], bt=case.block_tables, ctx=md["context_lens"])
         self.d = {k_: t(v_) for k_, v_ in self.host.items()}
         self.ws = pa.decode_workspace(len(case.num_cached), wl.n_heads, wl.n_kv_heads,
-                                      wl.head_dim, int(md["context_lens"].sum()), device=dev)
+                                      wl.head_dim, device=dev)
         self.out = torch.empty_like(self.d["q"])
         self.status = pa.new_status(dev)
         self.units = kv_bytes(case)

@@ -203,22 +203,25 @@ int pa_prefill_varlen(const void *q, const pa_cache_t *cache, int layer,
  * section 3; "nano-vllm notes - Llama", prepare_decode /
  * flash_attn_with_kvcache).  Sequence s has context_lens[s] cached tokens
  * (its new token's K/V already appended); its query attends to all of them:
- *     out[s][h] = softmax(q[s][h] . K^T * scale) V   over KV head h / g.
- * The context is cut into chunks of 256 tokens spread over the GPU; each
- * chunk's (max, sum, weighted V) is merged with the others by an online
- * softmax in the last chunk to finish.
+ *     out[s][h] = softmax(q[s][h] . K^T * scale) V   over KV head h / g,
+ * scores and softmax in fp32, P rounded to fp16 for P.V, fp16 out.
+ * The KV blocks of all (sequence, KV head) pairs are split into equal
+ * contiguous ranges, one per CTA of a persistent grid; a pair cut between
+ * ranges is finished by an online-softmax merge of its pieces.
  *   q             device fp16 [num_seqs][n_heads][head_dim] (rotated)
  *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
- *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq*block_size]
+ *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq*16]
+ *                 (others set PA_DEV_BAD_LENGTH and their output is not written)
  *   workspace     device, pa_decode_workspace_bytes(...) bytes, 256-byte
  *                 aligned, ZEROED by the caller before its first use; every
- *                 call leaves its counters at zero again.  One call at a time
- *                 per workspace.
+ *                 call leaves it ready for the next.  A smaller workspace (at
+ *                 least one CTA's records) only narrows the grid.  One call
+ *                 at a time per workspace.
  *   out           device fp16 [num_seqs][n_heads][head_dim]
- * total_context bounds sum(context_lens); it sizes the workspace.
+ *   scale         softmax scale; pass 0 for 1/sqrt(head_dim)
+ * Built for head_dim 64 and 128, n_heads / n_kv_heads <= 8, num_seqs <= 4096.
  */
-size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
-                                 int64_t total_context);
+size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads, int head_dim);
 int pa_decode(const void *q, const pa_cache_t *cache, int layer, const int32_t *block_tables,
               int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
               int n_heads, int n_kv_heads, int head_dim, float scale, void *workspace,

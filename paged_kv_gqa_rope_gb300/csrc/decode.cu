@@ -4,29 +4,34 @@
 // prepare_decode: context_lens include the token just appended;
 // "Meta Llama source deep-dive", 3.4 repeat_kv: Q head h reads KV head h/g).
 //
-// Work decomposition.  The context of sequence s is cut into chunks of 16
-// blocks (256 tokens).  A work item is (chunk, KV head); items are spread
-// round-robin over a persistent grid of CTAs.  Each CTA holds the prefix sum
-// of chunk counts in shared memory to map an item index to its sequence.
+// Work decomposition.  Every (sequence s, KV head h) pair owns
+// ceil(context_lens[s] / 16) KV blocks; laid end to end, pair after pair,
+// they form one line of W blocks.  The persistent grid of G CTAs cuts that
+// line into G equal ranges, so every CTA streams the same number of bytes
+// whatever the mix of context lengths.  A CTA walks its range as segments
+// (the part of one pair that falls in it).  A pair that lies inside one
+// range is finished there; a pair cut by range ends is finished by the CTA
+// that completes its last piece: each piece leaves (max, sum, unnormalised
+// O) in the workspace (record slot 0 if it is the CTA's first segment, 1 if
+// its last), and the last to arrive merges the 2-3 pieces by an online
+// softmax and resets the pair's arrival counter to zero.
 //
-// Inside a CTA one producer warp streams the item's K and V block tiles
-// (16 tokens x head_dim fp16 of one KV head, 4 KB each at d=128) with TMA into
-// a ring of shared-memory stages; four consumer warps take the blocks of the
-// item in turn.  Each warp computes, with warp-level tensor-core MMAs,
+// Inside a CTA one producer warp streams the K and V block tiles (16 tokens x
+// head_dim fp16 of one KV head) with TMA into a ring of shared-memory stages;
+// four consumer warps take the blocks of a segment in turn.  Each warp
+// computes, with warp-level tensor-core MMAs,
 //     S^T (16 tokens x 8 heads) = K (16 x d) . Q^T (d x 8 heads)
-// so the g Q heads that share the KV head form the N = 8 dimension and every
+// so the g Q heads that share the KV head form the N = 8 dimension and each
 // K/V byte is read once for the whole group; the online softmax runs on the
-// accumulator fragments with warp shuffles; P is rounded to fp16, transposed
-// in registers (movmatrix) and multiplied into
+// accumulator fragments with warp shuffles; P is rounded to fp16 (the row sum
+// accumulates the rounded values), transposed in registers (movmatrix) and
+// multiplied into
 //     O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads).
-// The four warps' (max, sum, O) are merged through shared memory.  A
-// sequence with one chunk writes its output directly; otherwise each chunk
-// stores (max, sum, O) in the workspace and the CTA that finishes the last
-// chunk of a (sequence, KV head) merges them (online-softmax reduction),
-// writes the output and resets the arrival counter to zero.
+// The four warps' (max, sum, O) are merged through shared memory at the end
+// of each segment.
 //
-// Bound: HBM.  Algorithmic bytes per sequence = context_len * Hk * d * 2 (K
-// and V) * 2 B.
+// Bound: HBM.  Algorithmic bytes = sum_s context_lens[s] * Hk * d * 2 (K, V)
+// * 2 B; everything else (Q, O, tables, partial records) is < 0.5 % of it.
 #include <mutex>
 
 #include "common.cuh"
@@ -35,48 +40,68 @@
 namespace pa {
 namespace {
 
-constexpr int kChunkBlocks = 16;
-constexpr int kChunkTokens = kChunkBlocks * kBlockSize;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSeqs = 4096;
-constexpr int kGroupPad = 8;  // MMA N: Q heads per KV head, padded
+constexpr int kGroupPad = 8;   // MMA N: Q heads per KV head, padded
+constexpr int kMaxGrid = 384;  // CTAs the workspace has record slots for
 
 struct DecodeArgs {
     const __half *q;              // [B][H][D]
     const int32_t *block_tables;  // [B][maxb]
     const int32_t *context_lens;  // [B]
     __half *out;                  // [B][H][D]
-    int32_t *counters;            // [B][Hk] arrival counters
-    float *part;                  // [cap][H][D + 4]: O (unnormalised), m, l
+    int32_t *counters;            // [B][Hk] arrival counters (zero between calls)
+    float *rec;                   // [grid][2][8][D + 4]: O (unnormalised), m, l
     int32_t *status;
     float scale_log2;             // scale * log2(e)
-    int B, H, Hk, g, maxb, num_blocks, plane_k, plane_v, cap_chunks;
+    int B, H, Hk, g, maxb, num_blocks, plane_k, plane_v;
 };
 
 template <int D>
 struct Layout {
     static constexpr int kTileBytes = kBlockSize * D * 2;  // one K or V block tile
     static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRec = D + 4;                     // floats per head record
 };
 
-__device__ __forceinline__ void item_of(int w, const int *prefix, int B, int Hk, int &s, int &kvh,
-                                        int &c) {
-    const int gc = w / Hk;
-    kvh = w - gc * Hk;
-    int lo = 0, hi = B - 1;
+// First block index of CTA c's range: floor(W * c / G).
+__device__ __forceinline__ int64_t range_start(int64_t W, int c, int G) { return W * c / G; }
+
+// The CTA whose range holds block index idx: the largest c with
+// floor(W c / G) <= idx, i.e. ceil((idx + 1) G / W) - 1.
+__device__ __forceinline__ int cta_of(int64_t idx, int64_t W, int G) {
+    return (int)(((idx + 1) * G + W - 1) / W) - 1;
+}
+
+// Segment of the block line starting at `pos` (< end): its pair and blocks.
+struct Segment {
+    int s, kvh, b0, nb, ctx;
+    int64_t pair_start, pair_end;
+};
+
+__device__ __forceinline__ Segment segment_at(int64_t pos, int64_t end, const int64_t *prefix,
+                                              int B, const int32_t *context_lens) {
+    int lo = 0, hi = B - 1;  // largest s with prefix[s] <= pos
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= gc)
+        if (prefix[mid] <= pos)
             lo = mid;
         else
             hi = mid - 1;
     }
-    s = lo;
-    c = gc - prefix[lo];
+    Segment g;
+    g.s = lo;
+    g.ctx = __ldg(context_lens + lo);
+    const int nblk = (g.ctx + kBlockSize - 1) / kBlockSize;
+    const int64_t rem = pos - prefix[lo];
+    g.kvh = (int)(rem / nblk);
+    g.b0 = (int)(rem - (int64_t)g.kvh * nblk);
+    g.pair_start = prefix[lo] + (int64_t)g.kvh * nblk;
+    g.pair_end = g.pair_start + nblk;
+    g.nb = (int)(min(end, g.pair_end) - pos);
+    return g;
 }
-
-__device__ __forceinline__ int chunks_of(int ctx) { return (ctx + kChunkTokens - 1) / kChunkTokens; }
 
 // Byte offset inside a K or V block tile written by TMA with 128-byte
 // swizzle: row r (token) of the tile holds D/64 lines of 128 B; line
@@ -103,19 +128,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
     float *sm_m = sm_o + kConsumerWarps * kGroupPad * D;           // [4][8]
     float *sm_l = sm_m + kConsumerWarps * kGroupPad;               // [4][8]
-    int *sm_flag = reinterpret_cast<int *>(sm_l + kConsumerWarps * kGroupPad);
-    int *prefix = sm_flag + 4;                                     // [B + 1]
+    int *sm_flag = reinterpret_cast<int *>(sm_l + kConsumerWarps * kGroupPad);  // [4]
+    int64_t *prefix = reinterpret_cast<int64_t *>(sm_flag + 4);    // [B + 1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
+    const int cta = blockIdx.x;
 
-    // -------- chunk counts and their prefix sum (every CTA, in smem)
+    // -------- blocks per sequence (all KV heads) and their prefix sum
     for (int s = tid; s < B; s += kThreads) {
         const int ctx = __ldg(a.context_lens + s);
-        int n = 0;
+        int64_t n = 0;
         if (ctx >= 1 && ctx <= a.maxb * kBlockSize)
-            n = chunks_of(ctx);
-        else if (blockIdx.x == 0)
+            n = (int64_t)((ctx + kBlockSize - 1) / kBlockSize) * a.Hk;
+        else if (cta == 0)
             report(a.status, PA_DEV_BAD_LENGTH);
         prefix[s + 1] = n;
     }
@@ -131,13 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (warp == 0) {  // inclusive scan of prefix[1..B] by one warp
-        int carry = 0;
+        int64_t carry = 0;
         for (int base = 1; base <= B; base += 32) {
             const int i = base + lane;
-            int v = i <= B ? prefix[i] : 0;
+            int64_t v = i <= B ? prefix[i] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                const int64_t t = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += t;
             }
             if (i <= B) prefix[i] = v + carry;
@@ -145,56 +171,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    const int total_chunks = prefix[B];
-    if (total_chunks > a.cap_chunks) {
-        if (blockIdx.x == 0 && tid == 0) report(a.status, PA_DEV_WORKSPACE);
-        return;
-    }
-    const int total_items = total_chunks * a.Hk;
+    const int64_t W = prefix[B];
+    // With fewer blocks than CTAs only the first W CTAs get a (one-block)
+    // range, so that every range is non-empty and a pair cut into pieces
+    // counts exactly one arrival per CTA between its first and last.
+    const int G = (int)(W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x);
+    if (cta >= G) return;
+    const int64_t start = range_start(W, cta, G), end = range_start(W, cta + 1, G);
 
     if (warp == kConsumerWarps) {
         // ================= producer warp: TMA block tiles into the ring
         if (lane == 0) tma_prefetch_desc(&kvmap);
         int gblk = 0;
         bool abort = false;
-        for (int w = blockIdx.x; w < total_items && !abort; w += gridDim.x) {
-            int s, kvh, c;
-            item_of(w, prefix, B, a.Hk, s, kvh, c);
-            const int ctx = __ldg(a.context_lens + s);
-            const int nblk_seq = (ctx + kBlockSize - 1) / kBlockSize;
-            const int b0 = c * kChunkBlocks;
-            const int nb = min(kChunkBlocks, nblk_seq - b0);
-            const int my_blk =
-                lane < nb ? __ldg(a.block_tables + (int64_t)s * a.maxb + b0 + lane) : 0;
-            for (int j = 0; j < nb; ++j) {
-                const int blk = __shfl_sync(0xffffffffu, my_blk, j);
-                const int stage = gblk % NSTAGE;
-                const uint32_t ph = (gblk / NSTAGE) & 1;
-                int ok = 1;
-                if (lane == 0) {
-                    ok = mbar_wait(&empty[stage], ph ^ 1);
-                    if (!ok) {
-                        report(a.status, PA_DEV_TIMEOUT);
-                    } else if (blk >= 0 && blk < a.num_blocks) {
-                        uint8_t *dst = stages + stage * L::kStageBytes;
-                        mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-                        tma_load_5d(dst, &kvmap, &full[stage], 0, 0, kvh, blk * kBlockSize,
-                                    a.plane_k);
-                        tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0, kvh,
-                                    blk * kBlockSize, a.plane_v);
-                    } else {
-                        report(a.status, PA_DEV_BAD_BLOCK);
-                        stage_bad[stage] = 1;
-                        mbar_arrive(&full[stage]);
+        for (int64_t pos = start; pos < end && !abort;) {
+            const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
+            const int32_t *row = a.block_tables + (int64_t)sg.s * a.maxb + sg.b0;
+            for (int w0 = 0; w0 < sg.nb && !abort; w0 += 32) {
+                const int cnt = min(32, sg.nb - w0);
+                const int my_blk = lane < cnt ? __ldg(row + w0 + lane) : 0;
+                for (int j = 0; j < cnt; ++j) {
+                    const int blk = __shfl_sync(0xffffffffu, my_blk, j);
+                    const int stage = gblk % NSTAGE;
+                    const uint32_t ph = (gblk / NSTAGE) & 1;
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = mbar_wait(&empty[stage], ph ^ 1);
+                        if (!ok) {
+                            report(a.status, PA_DEV_TIMEOUT);
+                        } else if (blk >= 0 && blk < a.num_blocks) {
+                            uint8_t *dst = stages + stage * L::kStageBytes;
+                            mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                            tma_load_5d(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
+                                        blk * kBlockSize, a.plane_k);
+                            tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0,
+                                        sg.kvh, blk * kBlockSize, a.plane_v);
+                        } else {
+                            report(a.status, PA_DEV_BAD_BLOCK);
+                            stage_bad[stage] = 1;
+                            mbar_arrive(&full[stage]);
+                        }
                     }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        abort = true;
+                        break;
+                    }
+                    ++gblk;
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    abort = true;
-                    break;
-                }
-                ++gblk;
             }
+            pos += sg.nb;
         }
         // Leave no copy in flight: wait (bounded) for the last stages issued.
         if (lane == 0) {
@@ -205,18 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================== consumer warps
-    const int head = lane >> 2;          // B-operand column (Q head in group)
+    const int head = lane >> 2;  // B-operand column (Q head in group)
     const int quad = lane & 3;
-    const int h0 = 2 * quad;             // accumulator columns held by this lane
+    const int h0 = 2 * quad;     // accumulator columns held by this lane
+    constexpr int kCons = kConsumerWarps * 32;
     int gblk = 0;
-    for (int w = blockIdx.x; w < total_items; w += gridDim.x) {
-        int s, kvh, c;
-        item_of(w, prefix, B, a.Hk, s, kvh, c);
-        const int ctx = __ldg(a.context_lens + s);
-        const int nblk_seq = (ctx + kBlockSize - 1) / kBlockSize;
-        const int b0 = c * kChunkBlocks;
-        const int nb = min(kChunkBlocks, nblk_seq - b0);
-        const int n_chunks = chunks_of(ctx);
+    for (int64_t pos = start; pos < end;) {
+        const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
+        const int s = sg.s, kvh = sg.kvh, b0 = sg.b0, nb = sg.nb, ctx = sg.ctx;
 
         // Q^T fragments (B operand): Q[head][16kk + 2*quad + {0,1}] and +8.
         uint32_t qb[D / 16][2];
@@ -278,6 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
                 const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
                 const int vrow = (lane & 7) + (lane >> 4) * 8;
+                // Rows of V past the context (the tail of a sequence's last
+                // block) are never written and may hold any bits, NaN
+                // included; P is 0 there, but 0 * NaN is not, so those
+                // tokens' lanes of the V^T fragment are cleared.
+                const int valid = ctx - (b0 + j) * kBlockSize;  // tokens in this block
+                uint32_t keep01 = 0xffffffffu, keep89 = 0xffffffffu;
+                if (valid < kBlockSize) {
+                    const int t0 = 2 * quad;
+                    keep01 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                    keep89 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+                }
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     o[mt][0] *= al0;
@@ -286,6 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o[mt][3] *= al1;
                     uint32_t af[4];
                     ldmatrix_x4_trans(af, vt + tile_offset<D>(vrow, mt * 2 + ((lane >> 3) & 1)));
+                    af[0] &= keep01;
+                    af[1] &= keep01;
+                    af[2] &= keep89;
+                    af[3] &= keep89;
                     mma_16816(o[mt], af, pb0, pb1);
                 }
             }
@@ -296,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // A timed-out wait leaves the ring out of step: every consumer warp
-        // learns of it at the barrier below and the CTA stops after this item.
+        // learns of it at the barrier below and the CTA stops after this segment.
         if (__any_sync(0xffffffffu, abort) && lane == 0) atomicOr(sm_flag + 1, 1);
         gblk += nb;
 
@@ -320,11 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ow[d + 8] = o[mt][2];
             ow[D + d + 8] = o[mt][3];
         }
-        named_barrier_sync(1, kConsumerWarps * 32);
+        named_barrier_sync(1, kCons);
         abort = sm_flag[1] != 0;
 
-        const int gc = prefix[s] + c;
-        for (int idx = tid; idx < a.g * D; idx += kConsumerWarps * 32) {
+        const bool whole = pos == sg.pair_start && pos + nb == sg.pair_end;
+        const int slot = pos == start ? 0 : 1;
+        float *myrec = a.rec + ((int64_t)(cta * 2 + slot) * kGroupPad) * L::kRec;
+        for (int idx = tid; idx < a.g * D; idx += kCons) {
             const int h = idx / D, d = idx - (idx / D) * D;
             float M = -INFINITY;
 #pragma unroll
@@ -338,52 +377,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     O += f * sm_o[(wv * kGroupPad + h) * D + d];
                 }
             }
-            const int hq = kvh * a.g + h;
-            if (n_chunks == 1) {
-                a.out[((int64_t)s * a.H + hq) * D + d] = __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
+            if (whole) {
+                a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
+                    __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
             } else {
-                float *rec = a.part + ((int64_t)gc * a.H + hq) * (D + 4);
-                rec[d] = O;
+                float *r = myrec + h * L::kRec;
+                r[d] = O;
                 if (d == 0) {
-                    rec[D] = M;
-                    rec[D + 1] = Lsum;
+                    r[D] = M;
+                    r[D + 1] = Lsum;
                 }
             }
         }
-        if (n_chunks > 1) {
+        if (!whole) {
             __threadfence();
-            named_barrier_sync(1, kConsumerWarps * 32);
+            named_barrier_sync(1, kCons);
+            const int c_first = cta_of(sg.pair_start, W, G);
+            const int c_last = cta_of(sg.pair_end - 1, W, G);
             if (tid == 0) {
                 const int prev = atomicAdd(a.counters + s * a.Hk + kvh, 1);
-                *sm_flag = (prev == n_chunks - 1);
+                sm_flag[0] = (prev == c_last - c_first);
             }
-            named_barrier_sync(1, kConsumerWarps * 32);
-            if (*sm_flag) {
+            named_barrier_sync(1, kCons);
+            if (sm_flag[0]) {
                 __threadfence();
-                const int gc0 = prefix[s];
-                for (int idx = tid; idx < a.g * D; idx += kConsumerWarps * 32) {
+                for (int idx = tid; idx < a.g * D; idx += kCons) {
                     const int h = idx / D, d = idx - (idx / D) * D;
-                    const int hq = kvh * a.g + h;
-                    const float *rec0 = a.part + ((int64_t)gc0 * a.H + hq) * (D + 4);
-                    const int64_t stride = (int64_t)a.H * (D + 4);
                     float M = -INFINITY;
-                    for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, __ldcg(rec0 + cc * stride + D));
+                    for (int c = c_first; c <= c_last; ++c) {
+                        const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                        const float *r = a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                        M = fmaxf(M, __ldcg(r + D));
+                    }
                     float O = 0.f, Lsum = 0.f;
                     if (M != -INFINITY) {
-                        for (int cc = 0; cc < n_chunks; ++cc) {
-                            const float *rec = rec0 + cc * stride;
-                            const float f = ex2(__ldcg(rec + D) - M);
-                            Lsum += f * __ldcg(rec + D + 1);
-                            O += f * __ldcg(rec + d);
+                        for (int c = c_first; c <= c_last; ++c) {
+                            const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                            const float *r =
+                                a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                            const float f = ex2(__ldcg(r + D) - M);
+                            Lsum += f * __ldcg(r + D + 1);
+                            O += f * __ldcg(r + d);
                         }
                     }
-                    a.out[((int64_t)s * a.H + hq) * D + d] =
+                    a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
                         __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
                 }
                 if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
             }
         }
-        named_barrier_sync(1, kConsumerWarps * 32);  // smem merge area free again
+        named_barrier_sync(1, kCons);  // the smem merge area is free again
+        pos += nb;
         if (abort) break;
     }
 }
@@ -392,13 +436,13 @@ template <int D, int NSTAGE>
 size_t decode_smem_bytes(int B) {
     return 1024 + (size_t)NSTAGE * Layout<D>::kStageBytes + 2 * NSTAGE * sizeof(uint64_t) +
            NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
-           4 * sizeof(int) + (size_t)(B + 1) * sizeof(int);
+           4 * sizeof(int) + 8 + (size_t)(B + 1) * sizeof(int64_t);
 }
 
 constexpr int kStages = 8;
 
 template <int D>
-int launch_decode(const CUtensorMap &map, const DecodeArgs &a, cudaStream_t st) {
+int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cudaStream_t st) {
     const size_t smem = decode_smem_bytes<D, kStages>(a.B);
     // The dynamic shared-memory limit and the occupancy depend only on the
     // device; both are set up once per device, on its first call.
@@ -425,13 +469,16 @@ int launch_decode(const CUtensorMap &map, const DecodeArgs &a, cudaStream_t st) 
         }
         per_sm = per_sm_of[dev];
     }
-    const int grid = sm_count() * per_sm;
+    const int grid = min(sm_count() * per_sm, max_grid);
+    if (grid < 1) return PA_ERR_CUDA;
     decode_kernel<D, kStages><<<grid, kThreads, smem, st>>>(map, a);
     return launch_status();
 }
 
-size_t counters_bytes(int B, int Hk) { return ((size_t)B * Hk * sizeof(int32_t) + 255) & ~(size_t)255; }
-size_t chunk_record_bytes(int H, int D) { return (size_t)H * (D + 4) * sizeof(float); }
+size_t counters_bytes(int B, int Hk) {
+    return ((size_t)B * Hk * sizeof(int32_t) + 255) & ~(size_t)255;
+}
+size_t cta_record_bytes(int D) { return (size_t)2 * kGroupPad * (D + 4) * sizeof(float); }
 
 }  // namespace
 }  // namespace pa
@@ -439,11 +486,9 @@ size_t chunk_record_bytes(int H, int D) { return (size_t)H * (D + 4) * sizeof(fl
 using namespace pa;
 
 extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
-                                            int head_dim, int64_t total_context) {
-    if (num_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || total_context < 0)
-        return 0;
-    const int64_t cap = num_seqs + (total_context + kChunkTokens - 1) / kChunkTokens;
-    return counters_bytes(num_seqs, n_kv_heads) + (size_t)cap * chunk_record_bytes(n_heads, head_dim);
+                                            int head_dim) {
+    if (num_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
+    return counters_bytes(num_seqs, n_kv_heads) + (size_t)kMaxGrid * cta_record_bytes(head_dim);
 }
 
 extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
@@ -462,8 +507,10 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PA_ERR_INVALID;
     const size_t cnt = counters_bytes(num_seqs, n_kv_heads);
-    if (workspace_bytes < cnt + chunk_record_bytes(n_heads, head_dim)) return PA_ERR_WORKSPACE;
-    const int64_t cap = (workspace_bytes - cnt) / chunk_record_bytes(n_heads, head_dim);
+    if (workspace_bytes < cnt + cta_record_bytes(head_dim)) return PA_ERR_WORKSPACE;
+    // A smaller workspace only narrows the grid.
+    const size_t slots = (workspace_bytes - cnt) / cta_record_bytes(head_dim);
+    const int max_grid = (int)(slots < (size_t)kMaxGrid ? slots : (size_t)kMaxGrid);
 
     CUtensorMap map;
     if (!make_cache_map(&map, cache, head_dim / 64, kBlockSize)) return PA_ERR_CUDA;
@@ -475,7 +522,7 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     a.context_lens = context_lens;
     a.out = static_cast<__half *>(out);
     a.counters = static_cast<int32_t *>(workspace);
-    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cnt);
+    a.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cnt);
     a.status = dev_status;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.B = num_seqs;
@@ -486,7 +533,7 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     a.num_blocks = cache->num_blocks;
     a.plane_k = layer;
     a.plane_v = cache->layers + layer;
-    a.cap_chunks = (int)(cap > INT32_MAX ? INT32_MAX : cap);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return head_dim == 128 ? launch_decode<128>(map, a, st) : launch_decode<64>(map, a, st);
+    return head_dim == 128 ? launch_decode<128>(map, a, max_grid, st)
+                           : launch_decode<64>(map, a, max_grid, st);
 }

@@ -57,7 +57,7 @@ _SIGS = {
                                 ctypes.POINTER(PaCache), _i32, _vp, _vp]),
     "pa_prefill_varlen": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _vp, _vp, _i32, _i32,
                                  _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
-    "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64]),
+    "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32, _i32,
                          _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
@@ -221,14 +221,14 @@ def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, ma
     return out
 
 
-def decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim, total_context) -> int:
-    return lib().pa_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim,
-                                           int(total_context))
+def decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim) -> int:
+    return lib().pa_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim)
 
 
-def decode_workspace(num_seqs, n_heads, n_kv_heads, head_dim, total_context, device="cuda"):
-    """A zeroed workspace for pa_decode (its counters must start at zero)."""
-    n = decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim, total_context)
+def decode_workspace(num_seqs, n_heads, n_kv_heads, head_dim, device="cuda", nbytes=None):
+    """A zeroed workspace for pa_decode (its counters must start at zero);
+    `nbytes` overrides the size (a smaller one narrows the grid)."""
+    n = decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim) if nbytes is None else nbytes
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 

@@ -63,9 +63,8 @@ class DecodeRun:
         self.slots = torch.from_numpy(md["slot_mapping"]).to(dev)
         self.ctx = torch.from_numpy(md["context_lens"]).to(dev)
         self.bt = torch.from_numpy(case.block_tables).to(dev)
-        total = int(md["context_lens"].sum())
         self.ws = pa.decode_workspace(len(case.num_cached), wl.n_heads, wl.n_kv_heads,
-                                      wl.head_dim, total)
+                                      wl.head_dim)
         self.status = pa.new_status()
 
     def run(self):

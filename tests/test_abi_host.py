@@ -35,8 +35,8 @@ def test_sizes(libpa):
     assert pa.cache_bytes(0, 16, 16, 2, 64) == 0
     assert libpa.pa_rope_table_bytes(100, 128) == 100 * 64 * 8
     assert libpa.pa_rope_table_bytes(100, 7) == 0
-    assert libpa.pa_decode_workspace_bytes(32, 64, 8, 128, 32 * 4097) > 0
-    assert libpa.pa_decode_workspace_bytes(0, 64, 8, 128, 10) == 0
+    assert libpa.pa_decode_workspace_bytes(32, 64, 8, 128) > 0
+    assert libpa.pa_decode_workspace_bytes(0, 64, 8, 128) == 0
 
 
 def test_cache_descriptor_wraps_caller_memory(libpa):

@@ -87,6 +87,9 @@ def test_decode_is_repeatable_and_resets_counters():
     assert torch.equal(out1, out2)
     ncnt = len(case.num_cached) * case.wl.n_kv_heads
     assert int(run.ws[:4 * ncnt].view(torch.int32).abs().sum().item()) == 0
+    # a workspace smaller than one CTA's records is refused on the host
+    with pytest.raises(pa.PAError):
+        pa.decode(run.q, run.cache, run.bt, run.ctx, run.ws[:256], case.wl.n_kv_heads)
 
 
 def test_decode_constant_v_returns_v():
@@ -96,6 +99,22 @@ def test_decode_constant_v_returns_v():
     run = DecodeRun(case, init)
     out = run.run()
     assert float((out.float() + 0.8125).abs().max()) < 1e-3
+
+
+def test_decode_ignores_nan_in_unwritten_slots():
+    """Slots past a sequence's context (the tail of its last block) may hold
+    any bits; NaN there must not reach the output."""
+    case, init = custom_case(16, 2, 128, [20, 300, 4], seed=12)
+    md = orc.decode_metadata(case.num_cached, case.block_tables, 16)
+    poisoned = init.copy()
+    for s, c in enumerate(case.num_cached):
+        n = int(c) + 1
+        blk = case.block_tables[s][(n - 1) // 16]
+        poisoned[:, 0, blk, n % 16 if n % 16 else 16:] = np.float16(np.nan)
+    run = DecodeRun(case, poisoned)
+    out = run.run()
+    _, _, _, want = oracle_decode_step(case, init)
+    assert_attention_close(out, want)
 
 
 def test_decode_bad_block_is_reported_not_read():
@@ -126,15 +145,28 @@ def test_decode_bad_context_is_reported():
     assert int(run.status.item()) & pa.PA_DEV_BAD_LENGTH
 
 
-def test_decode_workspace_overflow_is_reported():
-    case, init = custom_case(8, 2, 64, [2000, 3000], seed=10)
+@pytest.mark.parametrize("ctxs,Hk,ctas", [([2000, 3000], 2, 3), ([5000], 1, 5),
+                                           ([3, 7000, 40, 900, 16], 2, 7), ([300, 20], 2, 1),
+                                           ([1], 1, 2)])
+def test_decode_narrow_grid_merges_pieces(ctxs, Hk, ctas):
+    """A workspace with record slots for only a few CTAs narrows the grid, so
+    one (sequence, KV head) pair is cut into pieces across several CTAs and
+    merged; results must not change."""
+    H, d = 4 * Hk, 64
+    case, init = custom_case(H, Hk, d, ctxs, seed=sum(ctxs) + ctas)
     run = DecodeRun(case, init)
-    small = pa.decode_workspace(2, 8, 2, 64, 10)
-    run.status.zero_()
-    pa.rope_kv_write(run.q, run.k, run.v, run.positions, run.slots, run.table, run.cache)
-    pa.decode(run.q, run.cache, run.bt, run.ctx, small, 2, status=run.status)
+    full = pa.decode_workspace_bytes(len(ctxs), H, Hk, d)
+    slot_bytes = 2 * 8 * (d + 4) * 4
+    counters = (len(ctxs) * Hk * 4 + 255) // 256 * 256
+    assert full == counters + 384 * slot_bytes
+    run.ws = pa.decode_workspace(len(ctxs), H, Hk, d, nbytes=counters + ctas * slot_bytes)
+    out = run.run()
+    _, _, _, want = oracle_decode_step(case, init)
+    assert int(run.status.item()) == 0
+    assert_attention_close(out, want)
+    out2 = pa.decode(run.q, run.cache, run.bt, run.ctx, run.ws, Hk)   # counters were reset
     torch.cuda.synchronize()
-    assert int(run.status.item()) & pa.PA_DEV_WORKSPACE
+    assert torch.equal(out, out2)
 
 
 def test_rope_kv_write_prefill_workload_bit_exact():
