@@ -182,7 +182,8 @@ int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
  * n_kv_heads), all read from the cache through block_tables[s] (so the new
  * tokens' K/V must already have been written by pa_rope_kv_write):
  *     out = softmax(q k^T * scale) v,  scores and softmax in fp32, fp16 out.
- *   q            device fp16 [total_q][n_heads][head_dim] (rotated)
+ *   q            device fp16 [total_q][n_heads][head_dim] (rotated);
+ *                total_q = cu_seqlens_q[num_seqs], the rows of q and out
  *   cu_seqlens_q, cu_seqlens_k   device int32 [num_seqs + 1]
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
  *   max_seqlen_q host bound on any L_q (sizes the grid; longer sequences
@@ -192,7 +193,7 @@ int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
  * Built for head_dim 64 and 128 and any n_heads divisible by n_kv_heads;
  * Q.K^T and P.V run on the tcgen05 tensor cores with TMEM accumulators.
  */
-int pa_prefill_varlen(const void *q, const pa_cache_t *cache, int layer,
+int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *cache, int layer,
                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                       const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
                       int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,

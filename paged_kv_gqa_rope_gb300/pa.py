@@ -55,8 +55,8 @@ _SIGS = {
     "pa_rope_table_init": (_i32, [_vp, _i32, _i32, ctypes.c_double, _vp]),
     "pa_rope_kv_write": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32,
                                 ctypes.POINTER(PaCache), _i32, _vp, _vp]),
-    "pa_prefill_varlen": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _vp, _vp, _i32, _i32,
-                                 _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
+    "pa_prefill_varlen": (_i32, [_vp, _i32, ctypes.POINTER(PaCache), _i32, _vp, _vp, _vp, _i32,
+                                 _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32, _i32,
                          _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
@@ -215,7 +215,7 @@ def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, ma
     if out is None:
         out = torch.empty_like(q)
     _check("pa_prefill_varlen", lib().pa_prefill_varlen(
-        _p(q), ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
+        _p(q), T, ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
         _p(block_tables), block_tables.shape[1], cu_seqlens_q.shape[0] - 1, int(max_seqlen_q), H,
         n_kv_heads, d, float(scale), _p(out), _p(status), _stream(stream)))
     return out

@@ -105,6 +105,9 @@ def test_kernel_entry_points_validate_before_launch(libpa):
     assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 0, 4, 2, 64, 0.0, buf, 16, buf, None, None) == pa.PA_OK
     assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, 4, buf, 2, 4, 2, 64, -1.0, buf, 1 << 20, buf, None, None) == pa.PA_ERR_INVALID
     # prefill: H % Hk, head_dim
-    assert libpa.pa_prefill_varlen(buf, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 5, 2, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
-    assert libpa.pa_prefill_varlen(buf, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 96, 0.0, buf, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_prefill_varlen(buf, 8, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 5, 2, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_prefill_varlen(buf, 8, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 96, 0.0, buf, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert libpa.pa_prefill_varlen(buf, 8, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 4, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_prefill_varlen(buf, 0, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 64, 0.0, buf, None, None) == pa.PA_OK
+    assert libpa.pa_prefill_varlen(ctypes.c_void_p((1 << 24) + 8), 8, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
     assert libpa.pa_strerror(pa.PA_ERR_WORKSPACE) == b"decode workspace too small"
