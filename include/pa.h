@@ -228,6 +228,38 @@ int pa_decode(const void *q, const pa_cache_t *cache, int layer, const int32_t *
               int n_heads, int n_kv_heads, int head_dim, float scale, void *workspace,
               size_t workspace_bytes, void *out, int32_t *dev_status, pa_stream_t stream);
 
+/*
+ * pa_decode without a caller-supplied workspace.  The source pages have no
+ * counterpart to this entry point: it exists for callers that cannot hand
+ * the library device memory of their own, for example a plugin whose host
+ * framework owns every device allocation and gives the plugin none, or a
+ * caller that must not call cudaMalloc once it is running because of the
+ * device-wide synchronisation and the failure modes an allocation brings.
+ *
+ * The scratch memory pa_decode needs (arrival counters and the per-CTA
+ * partial records) lives instead in one fixed array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES bytes compiled into the library: every
+ * GPU that loads libpa holds that array until the process exits.  This
+ * entry point allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library call.  The first call on a device looks up the array's device
+ * address for that device (with that device current) and remembers it;
+ * make that first call before any stream capture starts.
+ *
+ * Arguments, results and device-side checks are those of pa_decode.  Each
+ * call clears the arrival counters in the array on `stream` before the
+ * kernel runs.  All calls in the process share the one array, so two calls
+ * that run at the same time on the GPU (on different streams, or from
+ * different threads) race and corrupt each other's results: serialise them.
+ * Returns PA_ERR_WORKSPACE when num_seqs * n_kv_heads is too large for the
+ * array (pa_decode_workspace_bytes(...) > PA_DECODE_NOALLOC_SCRATCH_BYTES).
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                      int head_dim, float scale, void *out, int32_t *dev_status,
+                      pa_stream_t stream);
+
 /* Human-readable text of a pa_status code. */
 const char *pa_strerror(int code);
 

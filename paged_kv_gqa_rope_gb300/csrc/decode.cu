@@ -537,3 +537,65 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     return head_dim == 128 ? launch_decode<128>(map, a, max_grid, st)
                            : launch_decode<64>(map, a, max_grid, st);
 }
+
+// ---------------------------------------------------------------- no-alloc variant
+//
+// For callers that cannot give the library device memory: the workspace of
+// pa_decode is taken from one fixed array of this translation unit.  Host
+// code never uses the array's name as an address (on the host it only
+// names a stand-in); the device address comes from cudaGetSymbolAddress,
+// looked up once per device with that device current.
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace pa {
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {nullptr};
+
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int num_seqs, int n_heads,
+                                 int n_kv_heads, int head_dim, float scale, void *out,
+                                 int32_t *dev_status, pa_stream_t stream) {
+    if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return PA_ERR_INVALID;
+    if (num_seqs == 0) return PA_OK;
+    const size_t need = pa_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim);
+    if (need == 0) return PA_ERR_INVALID;
+    if (need > PA_DECODE_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != PA_OK) return rc;
+    // Counters must start at zero; an earlier call that stopped early may
+    // have left some behind.
+    if (cudaMemsetAsync(scratch, 0, counters_bytes(num_seqs, n_kv_heads),
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return pa_decode(q, cache, layer, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     n_heads, n_kv_heads, head_dim, scale, scratch, need, out, dev_status, stream);
+}

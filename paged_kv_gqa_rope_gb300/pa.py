@@ -24,7 +24,7 @@ EXPORTS = (
     "pa_cache_bytes", "pa_alloc_cache", "pa_free_cache", "pa_prepare_prefill",
     "pa_prepare_decode", "pa_rope_table_bytes", "pa_rope_table_init", "pa_rope_kv_write",
     "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
-    "pa_check_device",
+    "pa_check_device", "pa_decode_noalloc",
 )
 
 
@@ -60,6 +60,8 @@ _SIGS = {
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32, _i32,
                          _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
+    "pa_decode_noalloc": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
+                                 _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
     "pa_check_device": (_i32, []),
 }
