@@ -117,6 +117,13 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int piece16) {
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeArgs a) {
+    // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
+    // with a barrier of all consumer warps.  With NSTAGE a multiple of the
+    // warp count, every use of a stage within a segment belongs to the same
+    // warp, so a warp never waits on a stage whose previous fill another warp
+    // has not consumed yet (the mbarrier parity would alias that wait onto
+    // the earlier, completed phase).
+    static_assert(NSTAGE % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -441,38 +448,48 @@ size_t decode_smem_bytes(int B) {
 
 constexpr int kStages = 8;
 
-template <int D>
-int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cudaStream_t st) {
-    const size_t smem = decode_smem_bytes<D, kStages>(a.B);
-    // The dynamic shared-memory limit and the occupancy depend only on the
-    // device; both are set up once per device, on its first call.
+template <int D, int NSTAGE>
+int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_grid,
+                         cudaStream_t st) {
+    const size_t smem = decode_smem_bytes<D, NSTAGE>(a.B);
+    // The kernel may use up to the shared memory of kMaxSeqs sequences; the
+    // limit is raised once per device.  The grid is sized from this call's
+    // shared memory, so small batches get more CTAs (bytes in flight) per SM.
     static std::mutex mu;
-    static int per_sm_of[64] = {0};
+    static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-    int per_sm;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (per_sm_of[dev] == 0) {
-            const size_t smax = decode_smem_bytes<D, kStages>(kMaxSeqs);
-            int n = 0;
-            if (cudaFuncSetAttribute(decode_kernel<D, kStages>,
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(decode_kernel<D, NSTAGE>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smax) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, kStages>,
-                                                              kThreads, smax) != cudaSuccess ||
-                n < 1) {
+                                     (int)decode_smem_bytes<D, NSTAGE>(kMaxSeqs)) != cudaSuccess) {
                 cudaGetLastError();
                 return PA_ERR_CUDA;
             }
-            per_sm_of[dev] = n;
+            attr_set[dev] = true;
         }
-        per_sm = per_sm_of[dev];
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NSTAGE>, kThreads,
+                                                      smem) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
     }
     const int grid = min(sm_count() * per_sm, max_grid);
     if (grid < 1) return PA_ERR_CUDA;
-    decode_kernel<D, kStages><<<grid, kThreads, smem, st>>>(map, a);
+    decode_kernel<D, NSTAGE><<<grid, kThreads, smem, st>>>(map, a);
     return launch_status();
+}
+
+template <int D>
+int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cudaStream_t st) {
+    // 8 stages of 8 KB at d=128 and two CTAs per SM (the register budget
+    // allows two) keep 128 KB of K/V in flight per SM; 4 stages, or 12-16
+    // stages at one CTA per SM, measured slower on all decode workloads.
+    return launch_decode_stages<D, kStages>(map, a, max_grid, st);
 }
 
 size_t counters_bytes(int B, int Hk) {
