@@ -6,27 +6,36 @@
 // Llama", prepare_prefill: cu_seqlens_q / cu_seqlens_k delimit the flattened
 // stream and block_tables locate every key, prefix and new, in the cache).
 //
-// One CTA computes one 128-row tile of queries of one sequence and one Q
-// head.  Row i of tile t sits at absolute position p + 128 t + i (p = cached
-// prefix length) and sees keys 0 .. p + 128 t + i; key tiles of 128 keys
-// (8 cache blocks) past the last row's position are never loaded, and only
-// the tiles that reach past the first row's position are masked.
+// Work unit: 256 query rows (two 128-row tiles) of one sequence and one Q
+// head.  Row i of a sequence with a cached prefix of p keys sits at
+// absolute position p + i and sees keys 0 .. p + i; key tiles of 64 keys
+// (4 cache blocks) past a tile's last row are never loaded, and only the
+// tiles that reach past a tile's first row are masked.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread i owns query row i, which is TMEM lane i;
-//   warp 4     producer: TMA loads of the Q tile and of the K / V tiles, one
-//              16-token block (x two 64-column halves) at a time, gathered
-//              through the block table into a 2-stage ring;
-//   warp 5     MMA issuer (one thread) and TMEM owner.
-// Tensor memory (512 columns): three 128-column score buffers S0..S2 and the
-// output accumulator O at column 384.  Per key tile j:
-//   S[j%3]  = Q . K_j^T                 tcgen05.mma, both operands in smem
-//   softmax reads S[j%3], writes P = 2^(s*scale*log2e - m) as fp16 over it
-//   O      += P . V_j                   tcgen05.mma, A = P from TMEM
-// The running maximum m only moves when a tile raises it by more than 8 (in
-// log2 units): P then stays <= 256 and O (in TMEM) is rescaled only on those
-// tiles, after the previous P.V has finished.  The row sum accumulates the
-// fp16-rounded P, so a constant V comes back exactly.
+// Schedule: units are ordered (sequence, head, row pair) and cut into equal
+// contiguous ranges of cost (key tiles to process), one per CTA of a
+// persistent grid, so the CTAs finish together and the units of one
+// (sequence, KV head) run back to back on one SM while their K/V is in L2.
+//
+// Roles (384 threads):
+//   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
+//   warps 4-7   softmax of query tile 1
+//   warp 8      producer: TMA loads of the two Q tiles and of the K / V
+//               tiles, one 16-token block x 64-column half at a time,
+//               gathered through the block table into a 3-stage ring
+//   warp 9      MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle
+// Tensor memory (512 columns): S0a S0b | S1a S1b | O0 | O1 (64 columns per
+// score buffer, head_dim per O).  Per key tile j, for each query tile t:
+//   S_t[j%2]  = Q_t . K_j^T     tcgen05.mma, both operands in shared memory
+//   softmax_t reads S_t[j%2], writes P = 2^(s*scale*log2e - m) as fp16 over it
+//   O_t      += P . V_j         tcgen05.mma, A = P from TMEM
+// Scores are double-buffered: S of tile j+2 is issued while the softmax
+// warps work on tile j, and a score buffer is rewritten only after the P.V
+// that read it two tiles earlier has completed.  The running maximum only
+// moves when a tile raises it by more than 8 (log2 units), so P <= 256 and O
+// is rescaled (in TMEM) only on those tiles.  The row sum accumulates the
+// fp16-rounded P.
 //
 // Bound: tensor cores.  Algorithmic FLOPs = 4 * d * H * (number of visible
 // (query, key) pairs).
@@ -40,15 +49,16 @@ namespace pa {
 namespace {
 
 constexpr int kBM = 128;  // query rows per tile
-constexpr int kBN = 128;  // keys per tile
+constexpr int kBN = 64;   // keys per tile
 constexpr int kBlocksPerTile = kBN / kBlockSize;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kUnitRows = 2 * kBM;
+constexpr int kStages = 3;  // K/V ring
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 12 * 32;  // 168 registers per thread, no spills
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 384;  // TMEM column of the O accumulator
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxSeqs = 2048;
 
 struct PrefillArgs {
     const int32_t *cu_q;
@@ -57,33 +67,41 @@ struct PrefillArgs {
     __half *out;
     int32_t *status;
     float scale_log2;
-    int B, H, g, maxb, num_blocks, plane_k, plane_v, tiles_max, total_q;
+    int B, H, g, maxb, num_blocks, plane_k, plane_v, max_seqlen_q, total_q;
 };
 
 template <int D>
 struct PL {
-    static constexpr int kHalf = kBM * 128;         // one 64-column half of a 128-row tile
-    static constexpr int kTile = kHalf * (D / 64);  // Q, K or V tile bytes
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTile;       // 2 stages
-    static constexpr int kV = kK + 2 * kTile;   // 2 stages
-    static constexpr int kBar = kV + 2 * kTile;
-    static constexpr int kBytes = kBar + 256;
+    static constexpr int kQHalf = kBM * 128;          // one 64-column half of a Q tile
+    static constexpr int kQTile = kQHalf * (D / 64);
+    static constexpr int kKVHalf = kBN * 128;         // one 64-column half of a K/V tile
+    static constexpr int kKVTile = kKVHalf * (D / 64);
+    static constexpr int kQ = 0;                      // 2 query tiles
+    static constexpr int kK = 2 * kQTile;             // kStages stages
+    static constexpr int kV = kK + kStages * kKVTile;
+    static constexpr int kBar = kV + kStages * kKVTile;
+    static constexpr int kPrefix = kBar + 512;        // int64 [B + 1]
+    static size_t bytes(int B) { return (size_t)kPrefix + (size_t)(B + 1) * 8; }
+    static constexpr int kOCol = 4 * kBN;             // O_t at kOCol + t * D
 };
 
-// barrier slots inside the barrier area
+// TMEM column of score buffer b of query tile t.
+__device__ __forceinline__ uint32_t s_col(int t, int b) { return (uint32_t)(t * 2 * kBN + b * kBN); }
+
 enum {
-    B_Q = 0,
-    B_KFULL = 1,    // 2
-    B_KEMPTY = 3,   // 2
-    B_VFULL = 5,    // 2
-    B_VEMPTY = 7,   // 2
-    B_VFIXED = 9,
-    B_SFULL = 10,   // 3
-    B_PREADY = 13,  // 3
-    B_ODONE = 16,   // 3
-    B_DRAIN = 19,
-    B_COUNT = 20
+    B_QFULL = 0,
+    B_QEMPTY = 1,
+    B_KFULL = 2,    // kStages
+    B_KEMPTY = 5,   // kStages
+    B_VFULL = 8,    // kStages
+    B_VEMPTY = 11,  // kStages
+    B_VFIXED = 14,
+    B_SFULL = 15,   // [tile][buffer]: 4
+    B_PREADY = 19,  // [tile][buffer]: 4
+    B_ODONE = 23,   // [tile][buffer]: 4
+    B_OFREE = 27,   // per tile: 2
+    B_DRAIN = 29,
+    B_COUNT = 30
 };
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -99,6 +117,121 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+// Shape of row pair k of a sequence with L_q query rows and a prefix of p.
+struct PairShape {
+    int rv[2];  // valid rows of query tile 0 / 1
+    int n[2];   // key tiles of query tile 0 / 1 (0 for an empty tile)
+    // Selects instead of a run-time index keep the shape in registers.
+    __device__ __forceinline__ int tiles(int t) const { return t ? n[1] : n[0]; }
+    __device__ __forceinline__ int rows(int t) const { return t ? rv[1] : rv[0]; }
+};
+
+__device__ __forceinline__ PairShape pair_shape(int p, int L_q, int k) {
+    PairShape ps;
+    const int q0 = k * kUnitRows;
+    ps.rv[0] = min(kBM, L_q - q0);
+    ps.rv[1] = max(0, min(kBM, L_q - q0 - kBM));
+    ps.n[0] = (p + q0 + ps.rv[0] + kBN - 1) / kBN;
+    ps.n[1] = ps.rv[1] > 0 ? (p + q0 + kBM + ps.rv[1] + kBN - 1) / kBN : 0;
+    return ps;
+}
+
+struct SeqInfo {
+    int q_begin, L_q, k_len;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const PrefillArgs &a, int s) {
+    SeqInfo si;
+    si.q_begin = __ldg(a.cu_q + s);
+    si.L_q = __ldg(a.cu_q + s + 1) - si.q_begin;
+    si.k_len = __ldg(a.cu_k + s + 1) - __ldg(a.cu_k + s);
+    return si;
+}
+
+__device__ __forceinline__ bool seq_ok(const PrefillArgs &a, const SeqInfo &si) {
+    return si.L_q >= 0 && si.k_len >= si.L_q && si.k_len <= a.maxb * kBlockSize &&
+           si.q_begin >= 0 && si.q_begin + si.L_q <= a.total_q;
+}
+
+// Walks the units (s, h, k) of one CTA's cost range in order.
+struct UnitIter {
+    int s, h, k;
+    int64_t start;  // cost offset of the current unit
+    SeqInfo si;
+    int p, npairs;
+    PairShape ps;
+
+    __device__ __forceinline__ void load_seq(const PrefillArgs &a) {
+        si = seq_info(a, s);
+        p = si.k_len - si.L_q;
+        npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
+    }
+    // Move to the first sequence at or after s that has any cost.
+    __device__ __forceinline__ void skip_empty(const PrefillArgs &a, const int64_t *prefix) {
+        while (s < a.B && prefix[s + 1] == prefix[s]) ++s;
+        if (s < a.B) {
+            load_seq(a);
+            ps = pair_shape(p, si.L_q, k);
+        }
+    }
+    // First unit whose start is >= x.
+    __device__ __forceinline__ void init(const PrefillArgs &a, const int64_t *prefix, int64_t x) {
+        const int64_t C = prefix[a.B];
+        h = 0;
+        k = 0;
+        if (x >= C) {
+            s = a.B;
+            start = C;
+            return;
+        }
+        int lo = 0, hi = a.B - 1;  // largest s with prefix[s] <= x
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        s = lo;
+        load_seq(a);
+        const int64_t hc = (prefix[s + 1] - prefix[s]) / a.H;
+        const int64_t off = x - prefix[s];
+        h = (int)(off / hc);
+        const int64_t rem = off - (int64_t)h * hc;
+        int64_t acc = 0;
+        while (acc < rem) {
+            const PairShape q = pair_shape(p, si.L_q, k);
+            acc += q.n[0] + q.n[1];
+            ++k;
+        }
+        start = prefix[s] + (int64_t)h * hc + acc;
+        if (k == npairs) {
+            k = 0;
+            if (++h == a.H) {
+                h = 0;
+                ++s;
+                skip_empty(a, prefix);
+                return;
+            }
+        }
+        ps = pair_shape(p, si.L_q, k);
+    }
+    __device__ __forceinline__ void next(const PrefillArgs &a, const int64_t *prefix) {
+        start += ps.n[0] + ps.n[1];
+        if (++k == npairs) {
+            k = 0;
+            if (++h == a.H) {
+                h = 0;
+                ++s;
+                skip_empty(a, prefix);
+                return;
+            }
+        }
+        ps = pair_shape(p, si.L_q, k);
+    }
+    __device__ __forceinline__ bool valid(int B, int64_t end) const { return s < B && start < end; }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -109,51 +242,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+    int64_t *prefix = reinterpret_cast<int64_t *>(smem + L::kPrefix);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B;
 
-    // ---- which tile: heavy (late) query tiles first, heads fastest
-    const int per_tile = a.H * a.B;
-    const int t = a.tiles_max - 1 - (int)(blockIdx.x / per_tile);
-    const int rem = (int)(blockIdx.x % per_tile);
-    const int s = rem / a.H, h = rem - (rem / a.H) * a.H;
-    const int q_begin = __ldg(a.cu_q + s), q_end = __ldg(a.cu_q + s + 1);
-    const int k_len = __ldg(a.cu_k + s + 1) - __ldg(a.cu_k + s);
-    const int L_q = q_end - q_begin;
-    if (L_q < 0 || k_len < L_q || k_len > a.maxb * kBlockSize || q_begin < 0 ||
-        q_end > a.total_q) {
-        if (t == 0 && h == 0 && tid == 0) report(a.status, PA_DEV_BAD_LENGTH);
-        return;
+    // ---- cost of every sequence (all heads) and its prefix sum
+    for (int s = tid; s < B; s += kThreads) {
+        const SeqInfo si = seq_info(a, s);
+        int64_t c = 0;
+        if (seq_ok(a, si)) {
+            const int p = si.k_len - si.L_q;
+            const int np = (si.L_q + kUnitRows - 1) / kUnitRows;
+            for (int k = 0; k < np; ++k) {
+                const PairShape ps = pair_shape(p, si.L_q, k);
+                c += ps.n[0] + ps.n[1];
+            }
+            if (si.L_q > a.max_seqlen_q && blockIdx.x == 0) report(a.status, PA_DEV_BAD_LENGTH);
+        } else if (blockIdx.x == 0) {
+            report(a.status, PA_DEV_BAD_LENGTH);
+        }
+        prefix[s + 1] = c * a.H;
     }
-    // Rows past the grid's tiles (L_q above the max_seqlen_q bound) are not
-    // computed; the sequence is reported.
-    if (L_q > a.tiles_max * kBM && t == 0 && h == 0 && tid == 0)
-        report(a.status, PA_DEV_BAD_LENGTH);
-    const int q0 = t * kBM;
-    if (q0 >= L_q) return;  // whole CTA
-
-    const int p = k_len - L_q;
-    const int rows_valid = min(kBM, L_q - q0);
-    const int kv_end = p + q0 + rows_valid;  // keys 0 .. kv_end-1 are visible to some row
-    const int n = (kv_end + kBN - 1) / kBN;
-    const int nblk_k = (k_len + kBlockSize - 1) / kBlockSize;
-    const int kvh = h / a.g;
-    const bool fix_tail = (k_len % kBlockSize) != 0 && (nblk_k - 1) / kBlocksPerTile == n - 1;
+    if (tid == 0) prefix[0] = 0;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t carry = 0;
+        for (int base = 1; base <= B; base += 32) {
+            const int i = base + lane;
+            int64_t v = i <= B ? prefix[i] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (i <= B) prefix[i] = v + carry;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+    const int64_t C = prefix[B];
+    const int G = gridDim.x;
+    const int64_t range_lo = C * blockIdx.x / G, range_hi = C * (blockIdx.x + 1) / G;
+    UnitIter first;
+    first.init(a, prefix, range_lo);
+    if (!first.valid(B, range_hi)) return;  // no unit starts in this range (whole CTA)
 
     if (tid == 0) {
-        mbar_init(&bar[B_Q], 1);
-        for (int i = 0; i < 2; ++i) {
+        mbar_init(&bar[B_QFULL], 1);
+        mbar_init(&bar[B_QEMPTY], 1);
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&bar[B_KFULL + i], 1);
             mbar_init(&bar[B_KEMPTY + i], 1);
             mbar_init(&bar[B_VFULL + i], 1);
             mbar_init(&bar[B_VEMPTY + i], 1);
         }
-        mbar_init(&bar[B_VFIXED], 1);
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&bar[B_SFULL + i], 1);
-            mbar_init(&bar[B_PREADY + i], kSoftmaxWarps * 32);
+            mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_ODONE + i], 1);
         }
+        mbar_init(&bar[B_OFREE + 0], 128);
+        mbar_init(&bar[B_OFREE + 1], 128);
+        mbar_init(&bar[B_VFIXED], 1);
         mbar_init(&bar[B_DRAIN], 1);
         fence_barrier_init();
     }
@@ -165,143 +316,198 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
-    if (warp == kProducerWarp) {
-        // ======================= producer: Q once, then K/V tiles
-        const int32_t *row = a.block_tables + (int64_t)s * a.maxb;
-        const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
-        auto block_row = [&](int j) -> int {            // cache row of lane's block in tile j
-            const int lb = j * kBlocksPerTile + lane;
-            if (lane >= kBlocksPerTile || lb >= nblk_k) return oob_row;
-            const int blk = __ldg(row + lb);
-            if (blk < 0 || blk >= a.num_blocks) {
-                report(a.status, PA_DEV_BAD_BLOCK);
-                return oob_row;
-            }
-            return blk * kBlockSize;
-        };
+    if (warp >= kProducerWarp) {
+      if (warp == kProducerWarp) {
+        // ======================= producer
         int ok = 1;
         if (lane == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kvmap);
-            mbar_arrive_expect_tx(&bar[B_Q], L::kTile);
-            for (int hf = 0; hf < D / 64; ++hf)
-                tma_load_4d(smem + L::kQ + hf * L::kHalf, &qmap, &bar[B_Q], 0, hf, h,
-                            q_begin + q0);
         }
-        int rows_cur = block_row(0);
-        int issued = 0;
-        for (int j = 0; j < n && ok; ++j) {
-            const int rows_next = j + 1 < n ? block_row(j + 1) : 0;
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
-            int r8[kBlocksPerTile];
-#pragma unroll
-            for (int b = 0; b < kBlocksPerTile; ++b) r8[b] = __shfl_sync(0xffffffffu, rows_cur, b);
-            if (lane == 0) {
-                ok = mbar_wait(&bar[B_KEMPTY + st], ph ^ 1);
-                if (ok) {
-                    uint8_t *kt = smem + L::kK + st * L::kTile;
-                    mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kTile);
-#pragma unroll
-                    for (int b = 0; b < kBlocksPerTile; ++b)
-                        for (int hf = 0; hf < D / 64; ++hf)
-                            tma_load_5d(kt + hf * L::kHalf + b * kBlockSize * 128, &kvmap,
-                                        &bar[B_KFULL + st], 0, hf, kvh, r8[b], a.plane_k);
-                    ok = mbar_wait(&bar[B_VEMPTY + st], ph ^ 1);
+        int kvc = 0, qc = 0;
+        for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix), ++qc) {
+            const int nmax = max(u.ps.n[0], u.ps.n[1]);
+            const int kvh = u.h / a.g;
+            const int q0 = u.k * kUnitRows;
+            const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
+            const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
+                                  (nblk_k - 1) / kBlocksPerTile == nmax - 1;
+            const int32_t *row = a.block_tables + (int64_t)u.s * a.maxb;
+            auto block_row = [&](int j) -> int {  // cache row of this lane's block of tile j
+                const int lb = j * kBlocksPerTile + lane;
+                if (lane >= kBlocksPerTile || lb >= nblk_k) return oob_row;
+                const int blk = __ldg(row + lb);
+                if (blk < 0 || blk >= a.num_blocks) {
+                    report(a.status, PA_DEV_BAD_BLOCK);
+                    return oob_row;
                 }
+                return blk * kBlockSize;
+            };
+            if (lane == 0) {
+                if (qc > 0) ok = mbar_wait(&bar[B_QEMPTY], (qc - 1) & 1);
                 if (ok) {
-                    uint8_t *vt = smem + L::kV + st * L::kTile;
-                    mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kTile);
-#pragma unroll
-                    for (int b = 0; b < kBlocksPerTile; ++b)
+                    const int ntiles = u.ps.rv[1] > 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(&bar[B_QFULL], L::kQTile * ntiles);
+                    for (int t = 0; t < ntiles; ++t)
                         for (int hf = 0; hf < D / 64; ++hf)
-                            tma_load_5d(vt + hf * L::kHalf + b * kBlockSize * 128, &kvmap,
-                                        &bar[B_VFULL + st], 0, hf, kvh, r8[b], a.plane_v);
+                            tma_load_4d(smem + L::kQ + t * L::kQTile + hf * L::kQHalf, &qmap,
+                                        &bar[B_QFULL], 0, hf, u.h, u.si.q_begin + q0 + t * kBM);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok && fix_tail && j == n - 1) {
-                // Rows of the sequence's last block past k_len are never
-                // written and may hold NaN bits; P is 0 there but 0 * NaN is
-                // not, so they are cleared before P.V reads the tile.
-                if (lane == 0) ok = mbar_wait(&bar[B_VFULL + st], ph);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) {
-                    uint8_t *vt = smem + L::kV + st * L::kTile;
-                    const int b_in = (nblk_k - 1) % kBlocksPerTile;
-                    const int r0 = k_len % kBlockSize;
-                    const int nrows = kBlockSize - r0;
-                    const int pieces = nrows * (D / 64) * 8;  // 16-byte pieces
-                    for (int i = lane; i < pieces; i += 32) {
-                        const int line = i >> 3, piece = i & 7;
-                        const int hf = line / nrows, r = r0 + line % nrows;
-                        *reinterpret_cast<uint4 *>(vt + hf * L::kHalf +
-                                                   (b_in * kBlockSize + r) * 128 + piece * 16) =
-                            make_uint4(0, 0, 0, 0);
+            int rows_cur = block_row(0);
+            for (int j = 0; j < nmax && ok; ++j) {
+                const int rows_next = j + 1 < nmax ? block_row(j + 1) : 0;
+                const int idx = kvc + j;
+                const int st = idx % kStages;
+                const uint32_t ph = (idx / kStages) & 1;
+                int rr[kBlocksPerTile];
+#pragma unroll
+                for (int b = 0; b < kBlocksPerTile; ++b)
+                    rr[b] = __shfl_sync(0xffffffffu, rows_cur, b);
+                if (lane == 0) {
+                    ok = mbar_wait(&bar[B_KEMPTY + st], ph ^ 1);
+                    if (ok) {
+                        uint8_t *kt = smem + L::kK + st * L::kKVTile;
+                        mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKVTile);
+#pragma unroll
+                        for (int b = 0; b < kBlocksPerTile; ++b)
+                            for (int hf = 0; hf < D / 64; ++hf)
+                                tma_load_5d(kt + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
+                                            &bar[B_KFULL + st], 0, hf, kvh, rr[b], a.plane_k);
+                        ok = mbar_wait(&bar[B_VEMPTY + st], ph ^ 1);
                     }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar[B_VFIXED]);
+                    if (ok) {
+                        uint8_t *vt = smem + L::kV + st * L::kKVTile;
+                        mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kKVTile);
+#pragma unroll
+                        for (int b = 0; b < kBlocksPerTile; ++b)
+                            for (int hf = 0; hf < D / 64; ++hf)
+                                tma_load_5d(vt + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
+                                            &bar[B_VFULL + st], 0, hf, kvh, rr[b], a.plane_v);
+                    }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok && fix_tail && j == nmax - 1) {
+                    // Rows of the sequence's last block past k_len are never
+                    // written and may hold NaN bits; P is 0 there but 0 * NaN
+                    // is not, so they are cleared before P.V reads the tile.
+                    if (lane == 0) ok = mbar_wait(&bar[B_VFULL + st], ph);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) {
+                        uint8_t *vt = smem + L::kV + st * L::kKVTile;
+                        const int b_in = (nblk_k - 1) % kBlocksPerTile;
+                        const int r0 = u.si.k_len % kBlockSize;
+                        const int nrows = kBlockSize - r0;
+                        const int pieces = nrows * (D / 64) * 8;  // 16-byte pieces
+                        for (int i = lane; i < pieces; i += 32) {
+                            const int line = i >> 3, piece = i & 7;
+                            const int hf = line / nrows, r = r0 + line % nrows;
+                            *reinterpret_cast<uint4 *>(vt + hf * L::kKVHalf +
+                                                       (b_in * kBlockSize + r) * 128 + piece * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[B_VFIXED]);
+                    }
+                }
+                rows_cur = rows_next;
             }
-            rows_cur = rows_next;
-            issued = j + 1;
+            kvc += nmax;
         }
         if (lane == 0) {
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             // Leave no copy in flight: the last tiles' loads have landed.
-            for (int j = max(0, issued - 2); j < issued; ++j) {
-                mbar_wait(&bar[B_KFULL + (j & 1)], (j >> 1) & 1);
-                mbar_wait(&bar[B_VFULL + (j & 1)], (j >> 1) & 1);
+            for (int i = max(0, kvc - kStages); i < kvc; ++i) {
+                mbar_wait(&bar[B_KFULL + i % kStages], (i / kStages) & 1);
+                mbar_wait(&bar[B_VFULL + i % kStages], (i / kStages) & 1);
             }
+            if (qc > 0) mbar_wait(&bar[B_QFULL], (qc - 1) & 1);
         }
-    } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp) {
         // ======================= MMA issuer (one thread)
         if (lane == 0) {
             constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN, false, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
-            const uint32_t q_base = smem_u32(smem + L::kQ);
-            bool ok = mbar_wait(&bar[B_Q], 0);
-            auto issue_s = [&](int jj) -> bool {
-                const int st = jj & 1;
-                if (!mbar_wait(&bar[B_KFULL + st], (jj >> 1) & 1)) return false;
+            bool ok = true;
+            int kvc = 0, qc = 0, fixc = 0;
+            int gt[2] = {0, 0};       // score tiles of query tile t issued in earlier units
+            int units_t[2] = {0, 0};  // earlier units with a non-empty tile t
+            // S_t for global score tile G into buffer G % 2, once the P.V that
+            // read that buffer (global tile G - 2) has completed.
+            auto issue_s = [&](int t, int G, int st) -> bool {
+                const int b = G & 1;
+                if (G >= 2 && !mbar_wait(&bar[B_ODONE + 2 * t + b], ((G - 2) >> 1) & 1))
+                    return false;
                 tc::fence_after();
-                const uint32_t k_base = smem_u32(smem + L::kK + st * L::kTile);
-                const uint32_t d_tmem = tmem + (jj % 3) * kBN;
+                const uint32_t q_base = smem_u32(smem + L::kQ + t * L::kQTile);
+                const uint32_t k_base = smem_u32(smem + L::kK + st * L::kKVTile);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-                    tc::mma_ss(d_tmem, tc::smem_desc_sw128(q_base + off, 16, 1024),
-                               tc::smem_desc_sw128(k_base + off, 16, 1024), kIdescQK, kk > 0);
-                }
-                tc::commit(&bar[B_SFULL + jj % 3]);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc::mma_ss(tmem + s_col(t, b),
+                               tc::smem_desc_sw128(q_base + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
+                                                   16, 1024),
+                               tc::smem_desc_sw128(k_base + (kk >> 2) * L::kKVHalf + (kk & 3) * 32,
+                                                   16, 1024),
+                               kIdescQK, kk > 0);
+                tc::commit(&bar[B_SFULL + 2 * t + b]);
+                return true;
+            };
+            // Both tiles' scores for key tile j of this unit (K from its stage).
+            auto issue_s_tile = [&](const UnitIter &u, int j) -> bool {
+                const int idx = kvc + j;
+                const int st = idx % kStages;
+                if (!mbar_wait(&bar[B_KFULL + st], (idx / kStages) & 1)) return false;
+                tc::fence_after();
+                if (j < u.ps.n[0] && !issue_s(0, gt[0] + j, st)) return false;
+                if (j < u.ps.n[1] && !issue_s(1, gt[1] + j, st)) return false;
                 tc::commit(&bar[B_KEMPTY + st]);
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
-            for (int j = 0; j < n && ok; ++j) {
-                const int b3 = j % 3, st = j & 1;
-                ok = mbar_wait(&bar[B_PREADY + b3], (j / 3) & 1);
-                if (!ok) break;
-                ok = (fix_tail && j == n - 1) ? mbar_wait(&bar[B_VFIXED], 0)
-                                              : mbar_wait(&bar[B_VFULL + st], (j >> 1) & 1);
-                if (!ok) break;
-                tc::fence_after();
-                const uint32_t v_base = smem_u32(smem + L::kV + st * L::kTile);
-                const uint32_t p_tmem = tmem + b3 * kBN;
+            for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix), ++qc) {
+                const int nmax = max(u.ps.n[0], u.ps.n[1]);
+                const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
+                const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
+                                      (nblk_k - 1) / kBlocksPerTile == nmax - 1;
+                ok = mbar_wait(&bar[B_QFULL], qc & 1);
+                if (ok) ok = issue_s_tile(u, 0);
+                if (ok && nmax > 1) ok = issue_s_tile(u, 1);
+                for (int j = 0; j < nmax && ok; ++j) {
+                    const int idx = kvc + j;
+                    const int st = idx % kStages;
+                    ok = (fix_tail && j == nmax - 1)
+                             ? mbar_wait(&bar[B_VFIXED], (fixc++) & 1)
+                             : mbar_wait(&bar[B_VFULL + st], (idx / kStages) & 1);
+                    tc::fence_after();
+                    const uint32_t v_base = smem_u32(smem + L::kV + st * L::kKVTile);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    tc::mma_ts(tmem + kOCol, p_tmem + kk * 8,
-                               tc::smem_desc_sw128(v_base + kk * 16 * 128, L::kHalf, 1024),
-                               kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                tc::commit(&bar[B_ODONE + b3]);
-                tc::commit(&bar[B_VEMPTY + st]);
-                if (j + 2 < n) {
-                    // S(j+2) overwrites the buffer P(j-1) was read from.
-                    if (j >= 1) ok = mbar_wait(&bar[B_ODONE + (j - 1) % 3], ((j - 1) / 3) & 1);
-                    if (ok) ok = issue_s(j + 2);
+                    for (int t = 0; t < 2; ++t) {
+                        if (!ok || j >= u.ps.n[t]) continue;
+                        const int G = gt[t] + j, b = G & 1;
+                        ok = mbar_wait(&bar[B_PREADY + 2 * t + b], (G >> 1) & 1);
+                        if (ok && j == 0 && units_t[t] > 0)
+                            ok = mbar_wait(&bar[B_OFREE + t], (units_t[t] - 1) & 1);
+                        tc::fence_after();
+                        if (!ok) continue;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t, b) + kk * 8,
+                                       tc::smem_desc_sw128(v_base + kk * 16 * 128, L::kKVHalf, 1024),
+                                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc::commit(&bar[B_ODONE + 2 * t + b]);
+                    }
+                    tc::commit(&bar[B_VEMPTY + st]);
+                    if (ok && j + 2 < nmax) ok = issue_s_tile(u, j + 2);
+                }
+                kvc += nmax;
+                tc::commit(&bar[B_QEMPTY]);  // completes once every MMA of this unit has
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    gt[t] += u.ps.n[t];
+                    if (u.ps.n[t] > 0) ++units_t[t];
                 }
             }
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
@@ -310,89 +516,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar[B_DRAIN], 0);
         }
         __syncwarp();
+      }
     } else {
-        // ======================= softmax warps: thread = query row
-        const int r = tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const int apos = p + q0 + r;
-        const int key_lim = min(apos, k_len - 1);  // last key this row may see
+        // ======================= softmax warpgroups: thread = query row
+        const int t = warp >> 2;      // query tile of this warpgroup
+        const int r = tid - t * 128;  // row in the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t o_tmem = tmem + lane_base + L::kOCol + t * D;
         const float sl2 = a.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int b3 = j % 3;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + b3], (j / 3) & 1));
-            if (!ok) break;
-            tc::fence_after();
-            const uint32_t s_tmem = tmem + lane_base + b3 * kBN;
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::ld32(s_tmem + c * 32, sr[c]);
-            float mx = -INFINITY;
-            const bool masked = j * kBN + kBN - 1 > p + q0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (masked && j * kBN + c * 32 + i > key_lim) sr[c][i] = f2u(-INFINITY);
-                    mx = fmaxf(mx, u2f(sr[c][i]));
-                }
-            }
-            const float m_tile = mx * sl2;
-            const bool raise = m_tile > m_used + kRescaleThreshold;
-            float alpha = 1.f;
-            if (raise) {
-                alpha = ex2(m_used - m_tile);  // 0 on the first tile
-                l *= alpha;
-                m_used = m_tile;
-            }
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                // O must hold P(j-1).V(j-1) before it is scaled.
+        int g = 0;  // score tiles of this query tile in earlier units
+        for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix)) {
+            const int n = u.ps.tiles(t);
+            if (n == 0) continue;
+            const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
+            const int key_lim = min(first_row + r, u.si.k_len - 1);
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                const int G = g + j, b = G & 1;
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bar[B_ODONE + (j - 1) % 3], ((j - 1) / 3) & 1));
+                                mbar_wait(&bar[B_SFULL + 2 * t + b], (G >> 1) & 1));
                 if (!ok) break;
                 tc::fence_after();
-                const uint32_t o_tmem = tmem + lane_base + kOCol;
+                const uint32_t s_tmem = tmem + lane_base + s_col(t, b);
+                uint32_t sr[2][32];
+                tc::ld32(s_tmem, sr[0]);
+                tc::ld32(s_tmem + 32, sr[1]);
+                float mx = -INFINITY;
+                const bool masked = j * kBN + kBN - 1 > first_row;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t orr[32];
-                    tc::ld32(o_tmem + c * 32, orr);
+                for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * alpha);
-                    tc::st32(o_tmem + c * 32, orr);
+                    for (int i = 0; i < 32; ++i) {
+                        if (masked && j * kBN + c * 32 + i > key_lim) sr[c][i] = f2u(-INFINITY);
+                        mx = fmaxf(mx, u2f(sr[c][i]));
+                    }
                 }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(u2f(sr[c][2 * i]), sl2, -m_used));
-                    const float p1 = ex2(fmaf(u2f(sr[c][2 * i + 1]), sl2, -m_used));
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    l += __low2float(hp) + __high2float(hp);
-                    pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                const float m_tile = mx * sl2;
+                const bool raise = m_tile > m_used + kRescaleThreshold;
+                float alpha = 1.f;
+                if (raise) {
+                    alpha = ex2(m_used - m_tile);  // 0 on the first tile
+                    l *= alpha;
+                    m_used = m_tile;
                 }
-                tc::st16(s_tmem + c * 16, pk);
+                if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                    // O_t must hold the previous tile's P.V before it is scaled.
+                    const int Gp = G - 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + 2 * t + (Gp & 1)],
+                                                           (Gp >> 1) & 1));
+                    if (!ok) break;
+                    tc::fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t orr[32];
+                        tc::ld32(o_tmem + c * 32, orr);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * alpha);
+                        tc::st32(o_tmem + c * 32, orr);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(u2f(sr[c][2 * i]), sl2, -m_used));
+                        const float p1 = ex2(fmaf(u2f(sr[c][2 * i + 1]), sl2, -m_used));
+                        const __half2 hp = __floats2half2_rn(p0, p1);
+                        l += __low2float(hp) + __high2float(hp);
+                        pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                    }
+                    tc::st16(s_tmem + c * 16, pk);
+                }
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(&bar[B_PREADY + 2 * t + b]);
             }
-            tc::wait_st();
-            tc::fence_before();
-            mbar_arrive(&bar[B_PREADY + b3]);
-        }
-        if (ok)
+            if (!ok) break;
+            const int Gl = g + n - 1;
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bar[B_ODONE + (n - 1) % 3], ((n - 1) / 3) & 1));
-        if (ok) {
+                            mbar_wait(&bar[B_ODONE + 2 * t + (Gl & 1)], (Gl >> 1) & 1));
+            if (!ok) break;
             tc::fence_after();
-            const uint32_t o_tmem = tmem + lane_base + kOCol;
+            const bool row_valid = r < u.ps.rows(t);
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(a.out +
-                                                   ((int64_t)(q_begin + q0 + r) * a.H + h) * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.out + ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
                 tc::ld32(o_tmem + c * 32, orr);
-                if (r < rows_valid) {
+                if (row_valid) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         uint32_t w[4];
@@ -406,9 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (lane == 0) {
-            report(a.status, PA_DEV_TIMEOUT);
+            tc::fence_before();
+            mbar_arrive(&bar[B_OFREE + t]);  // O_t has been read: the next unit may overwrite it
+            g += n;
         }
+        if (!ok && lane == 0) report(a.status, PA_DEV_TIMEOUT);
     }
 
     tc::fence_before();
@@ -417,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tc::dealloc(tmem, kTmemCols);
 }
 
-// 4-D fp16 map of q or out [T][H][D]: {64, D/64, H, T}, box {64, 1, 1, 128}.
+// 4-D fp16 map of q [T][H][D]: {64, D/64, H, T}, box {64, 1, 1, 128}.
 bool make_rows_map(CUtensorMap *map, const void *base, int T, int H, int D) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
@@ -434,27 +651,29 @@ bool make_rows_map(CUtensorMap *map, const void *base, int T, int H, int D) {
 template <int D>
 int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
                    cudaStream_t st) {
-    // At least 116 KB of shared memory keeps one CTA per SM, so no CTA
-    // waits in tcgen05.alloc for another's 512 TMEM columns.
-    const size_t smem = (PL<D>::kBytes > 116 * 1024 ? PL<D>::kBytes : 116 * 1024) + 1024;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    // At least 116 KB of shared memory keeps one CTA per SM, so no CTA waits
+    // in tcgen05.alloc for another's 512 TMEM columns.
+    const size_t smax = PL<D>::bytes(kMaxSeqs) + 1024;
+    const size_t need = PL<D>::bytes(a.B) + 1024;
+    const size_t smem = need > 116 * 1024 ? need : 116 * 1024;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
             if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess) {
+                                     (int)(smax > 116 * 1024 ? smax : 116 * 1024)) != cudaSuccess) {
                 cudaGetLastError();
                 return PA_ERR_CUDA;
             }
             attr_set[dev] = true;
         }
     }
-    const int64_t grid = (int64_t)a.tiles_max * a.H * a.B;
-    if (grid > 0x7fffffff) return PA_ERR_UNSUPPORTED;
-    prefill_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(qmap, kvmap, a);
+    const int grid = sm_count();
+    if (grid < 1) return PA_ERR_CUDA;
+    prefill_kernel<D><<<grid, kThreads, smem, st>>>(qmap, kvmap, a);
     return launch_status();
 }
 
@@ -473,6 +692,7 @@ extern "C" int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *c
         total_q < 0 || max_seqlen_q < 0 || max_blocks_per_seq <= 0 || !(scale >= 0.f))
         return PA_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
     if (!cache_ok(cache, layer, n_kv_heads, head_dim)) return PA_ERR_INVALID;
     if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return PA_OK;
     if (!q || !out || !cu_seqlens_q || !cu_seqlens_k || !block_tables) return PA_ERR_INVALID;
@@ -498,7 +718,7 @@ extern "C" int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *c
     a.num_blocks = cache->num_blocks;
     a.plane_k = layer;
     a.plane_v = cache->layers + layer;
-    a.tiles_max = (max_seqlen_q + kBM - 1) / kBM;
+    a.max_seqlen_q = max_seqlen_q;
     a.total_q = total_q;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch_prefill<128>(qmap, kvmap, a, st)
