@@ -8,8 +8,8 @@
 //
 // Work unit: 256 query rows (two 128-row tiles) of one sequence and one Q
 // head.  Row i of a sequence with a cached prefix of p keys sits at
-// absolute position p + i and sees keys 0 .. p + i; key tiles of 64 keys
-// (4 cache blocks) past a tile's last row are never loaded, and only the
+// absolute position p + i and sees keys 0 .. p + i; key tiles of 128 keys
+// (8 cache blocks) past a tile's last row are never loaded, and only the
 // tiles that reach past a tile's first row are masked.
 //
 // Schedule: units are ordered (sequence, head, row pair) and cut into equal
@@ -20,22 +20,24 @@
 // Roles (384 threads):
 //   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
 //   warps 4-7   softmax of query tile 1
-//   warp 8      producer: TMA loads of the two Q tiles and of the K / V
-//               tiles, one 16-token block x 64-column half at a time,
-//               gathered through the block table into a 3-stage ring
+//   warp 8      producer of the two Q tiles and the K tiles, warp 10 of the
+//               V tiles: TMA loads of one 16-token block x 64-column half
+//               at a time, gathered through the block table into 2-stage
+//               rings, each refilled as soon as its own slot is free
 //   warp 9      MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle
-// Tensor memory (512 columns): S0a S0b | S1a S1b | O0 | O1 (64 columns per
-// score buffer, head_dim per O).  Per key tile j, for each query tile t:
-//   S_t[j%2]  = Q_t . K_j^T     tcgen05.mma, both operands in shared memory
-//   softmax_t reads S_t[j%2], writes P = 2^(s*scale*log2e - m) as fp16 over it
-//   O_t      += P . V_j         tcgen05.mma, A = P from TMEM
-// Scores are double-buffered: S of tile j+2 is issued while the softmax
-// warps work on tile j, and a score buffer is rewritten only after the P.V
-// that read it two tiles earlier has completed.  The running maximum only
-// moves when a tile raises it by more than 8 (log2 units), so P <= 256 and O
-// is rescaled (in TMEM) only on those tiles.  The row sum accumulates the
-// fp16-rounded P.
+//   warp 11     idle
+// Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
+// tile, head_dim per O).  Per key tile j the MMA thread issues, in order,
+//   O0 += P0 . V_j   (A = P0 from TMEM, once softmax_0 wrote it over S0)
+//   S0  = Q0 . K_j+1^T (after that P.V has completed: same TMEM)
+//   O1 += P1 . V_j,  S1 = Q1 . K_j+1^T
+// so softmax_0 works on S0(j+1) while the tensor core runs tile 1's MMAs and
+// softmax_1 while it runs tile 0's.  Every MMA has N = 128 (M = 128, K = 16):
+// a tcgen05.mma takes about 96 cycles at any N up to 128, so wide tiles use
+// the tensor core better.  The running maximum only moves when a tile raises
+// it by more than 8 (log2 units), so P <= 256 and O is rescaled (in TMEM)
+// only on those tiles.  The row sum adds P in fp32 before its rounding to
+// fp16 (the two differ by far less than the output's own fp16 rounding).
 //
 // Bound: tensor cores.  Algorithmic FLOPs = 4 * d * H * (number of visible
 // (query, key) pairs).
@@ -49,12 +51,13 @@ namespace pa {
 namespace {
 
 constexpr int kBM = 128;  // query rows per tile
-constexpr int kBN = 64;   // keys per tile
+constexpr int kBN = 128;  // keys per tile
 constexpr int kBlocksPerTile = kBN / kBlockSize;
 constexpr int kUnitRows = 2 * kBM;
-constexpr int kStages = 3;  // K/V ring
+constexpr int kStages = 2;  // K/V ring
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;
 constexpr int kThreads = 12 * 32;  // 168 registers per thread, no spills
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
@@ -82,26 +85,26 @@ struct PL {
     static constexpr int kBar = kV + kStages * kKVTile;
     static constexpr int kPrefix = kBar + 512;        // int64 [B + 1]
     static size_t bytes(int B) { return (size_t)kPrefix + (size_t)(B + 1) * 8; }
-    static constexpr int kOCol = 4 * kBN;             // O_t at kOCol + t * D
+    static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
 };
 
-// TMEM column of score buffer b of query tile t.
-__device__ __forceinline__ uint32_t s_col(int t, int b) { return (uint32_t)(t * 2 * kBN + b * kBN); }
+// TMEM column of the score tile of query tile t.
+__device__ __forceinline__ uint32_t s_col(int t) { return (uint32_t)(t * kBN); }
 
 enum {
     B_QFULL = 0,
     B_QEMPTY = 1,
     B_KFULL = 2,    // kStages
-    B_KEMPTY = 5,   // kStages
-    B_VFULL = 8,    // kStages
-    B_VEMPTY = 11,  // kStages
-    B_VFIXED = 14,
-    B_SFULL = 15,   // [tile][buffer]: 4
-    B_PREADY = 19,  // [tile][buffer]: 4
-    B_ODONE = 23,   // [tile][buffer]: 4
-    B_OFREE = 27,   // per tile: 2
-    B_DRAIN = 29,
-    B_COUNT = 30
+    B_KEMPTY = 4,   // kStages
+    B_VFULL = 6,    // kStages
+    B_VEMPTY = 8,   // kStages
+    B_VFIXED = 10,  // kStages: a V tile whose tail rows were cleared
+    B_SFULL = 12,   // per query tile
+    B_PREADY = 14,  // per query tile
+    B_ODONE = 16,   // per query tile
+    B_OFREE = 18,   // per query tile
+    B_DRAIN = 20,
+    B_COUNT = 21
 };
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -296,15 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_KEMPTY + i], 1);
             mbar_init(&bar[B_VFULL + i], 1);
             mbar_init(&bar[B_VEMPTY + i], 1);
+            mbar_init(&bar[B_VFIXED + i], 1);
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bar[B_SFULL + i], 1);
             mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_ODONE + i], 1);
+            mbar_init(&bar[B_OFREE + i], 128);
         }
-        mbar_init(&bar[B_OFREE + 0], 128);
-        mbar_init(&bar[B_OFREE + 1], 128);
-        mbar_init(&bar[B_VFIXED], 1);
         mbar_init(&bar[B_DRAIN], 1);
         fence_barrier_init();
     }
@@ -319,11 +321,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
     if (warp >= kProducerWarp) {
-      if (warp == kProducerWarp) {
-        // ======================= producer
+      if (warp == kProducerWarp || warp == kVProducerWarp) {
+        // ======================= producers: Q and K tiles (warp 8), V tiles
+        // (warp 10), each as soon as its own ring has room
+        const bool is_v = warp == kVProducerWarp;
+        const int full0 = is_v ? B_VFULL : B_KFULL;
+        const int empty0 = is_v ? B_VEMPTY : B_KEMPTY;
+        const int plane = is_v ? a.plane_v : a.plane_k;
+        uint8_t *const ring = smem + (is_v ? L::kV : L::kK);
         int ok = 1;
         if (lane == 0) {
-            tma_prefetch_desc(&qmap);
+            if (!is_v) tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kvmap);
         }
         int kvc = 0, qc = 0;
@@ -332,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
             const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
-            const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
+            const bool fix_tail = is_v && (u.si.k_len % kBlockSize) != 0 &&
                                   (nblk_k - 1) / kBlocksPerTile == nmax - 1;
             const int32_t *row = a.block_tables + (int64_t)u.s * a.maxb;
             auto block_row = [&](int j) -> int {  // cache row of this lane's block of tile j
@@ -340,12 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane >= kBlocksPerTile || lb >= nblk_k) return oob_row;
                 const int blk = __ldg(row + lb);
                 if (blk < 0 || blk >= a.num_blocks) {
-                    report(a.status, PA_DEV_BAD_BLOCK);
+                    if (!is_v) report(a.status, PA_DEV_BAD_BLOCK);
                     return oob_row;
                 }
                 return blk * kBlockSize;
             };
-            if (lane == 0) {
+            if (!is_v && lane == 0) {
                 if (qc > 0) ok = mbar_wait(&bar[B_QEMPTY], (qc - 1) & 1);
                 if (ok) {
                     const int ntiles = u.ps.rv[1] > 0 ? 2 : 1;
@@ -368,25 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < kBlocksPerTile; ++b)
                     rr[b] = __shfl_sync(0xffffffffu, rows_cur, b);
                 if (lane == 0) {
-                    ok = mbar_wait(&bar[B_KEMPTY + st], ph ^ 1);
+                    ok = mbar_wait(&bar[empty0 + st], ph ^ 1);
                     if (ok) {
-                        uint8_t *kt = smem + L::kK + st * L::kKVTile;
-                        mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKVTile);
+                        uint8_t *dst = ring + st * L::kKVTile;
+                        mbar_arrive_expect_tx(&bar[full0 + st], L::kKVTile);
 #pragma unroll
                         for (int b = 0; b < kBlocksPerTile; ++b)
                             for (int hf = 0; hf < D / 64; ++hf)
-                                tma_load_5d(kt + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
-                                            &bar[B_KFULL + st], 0, hf, kvh, rr[b], a.plane_k);
-                        ok = mbar_wait(&bar[B_VEMPTY + st], ph ^ 1);
-                    }
-                    if (ok) {
-                        uint8_t *vt = smem + L::kV + st * L::kKVTile;
-                        mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kKVTile);
-#pragma unroll
-                        for (int b = 0; b < kBlocksPerTile; ++b)
-                            for (int hf = 0; hf < D / 64; ++hf)
-                                tma_load_5d(vt + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
-                                            &bar[B_VFULL + st], 0, hf, kvh, rr[b], a.plane_v);
+                                tma_load_5d(dst + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
+                                            &bar[full0 + st], 0, hf, kvh, rr[b], plane);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -411,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc::fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar[B_VFIXED]);
+                        if (lane == 0) mbar_arrive(&bar[B_VFIXED + st]);
                     }
                 }
                 rows_cur = rows_next;
@@ -421,11 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             // Leave no copy in flight: the last tiles' loads have landed.
-            for (int i = max(0, kvc - kStages); i < kvc; ++i) {
-                mbar_wait(&bar[B_KFULL + i % kStages], (i / kStages) & 1);
-                mbar_wait(&bar[B_VFULL + i % kStages], (i / kStages) & 1);
-            }
-            if (qc > 0) mbar_wait(&bar[B_QFULL], (qc - 1) & 1);
+            for (int i = max(0, kvc - kStages); i < kvc; ++i)
+                mbar_wait(&bar[full0 + i % kStages], (i / kStages) & 1);
+            if (!is_v && qc > 0) mbar_wait(&bar[B_QFULL], (qc - 1) & 1);
         }
       } else if (warp == kMmaWarp) {
         // ======================= MMA issuer (one thread)
@@ -433,27 +429,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN, false, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
             bool ok = true;
-            int kvc = 0, qc = 0, fixc = 0;
-            int gt[2] = {0, 0};       // score tiles of query tile t issued in earlier units
+            int kvc = 0, qc = 0;
+            int fixc0 = 0, fixc1 = 0;  // cleared V tiles of ring stage 0 / 1
+            int gt[2] = {0, 0};       // score tiles of query tile t in earlier units
             int units_t[2] = {0, 0};  // earlier units with a non-empty tile t
-            // S_t for global score tile G into buffer G % 2, once the P.V that
-            // read that buffer (global tile G - 2) has completed.
+            // Shared-memory descriptors of every operand buffer, built once; a
+            // k-step only adds its byte offset / 16 to the start-address field.
+            const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+            const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(smem + L::kV), L::kKVHalf, 1024);
+            // S_t for global score tile G, once the P.V of tile G - 1 (which
+            // read the same TMEM) has completed.
             auto issue_s = [&](int t, int G, int st) -> bool {
-                const int b = G & 1;
-                if (G >= 2 && !mbar_wait(&bar[B_ODONE + 2 * t + b], ((G - 2) >> 1) & 1))
-                    return false;
+                if (G >= 1 && !mbar_wait(&bar[B_ODONE + t], (G - 1) & 1)) return false;
                 tc::fence_after();
-                const uint32_t q_base = smem_u32(smem + L::kQ + t * L::kQTile);
-                const uint32_t k_base = smem_u32(smem + L::kK + st * L::kKVTile);
+                const uint64_t dq = dq0 + (uint64_t)((t * L::kQTile) >> 4);
+                const uint64_t dk = dk0 + (uint64_t)((st * L::kKVTile) >> 4);
+                const uint32_t d_tmem = tmem + s_col(t);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc::mma_ss(tmem + s_col(t, b),
-                               tc::smem_desc_sw128(q_base + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
-                                                   16, 1024),
-                               tc::smem_desc_sw128(k_base + (kk >> 2) * L::kKVHalf + (kk & 3) * 32,
-                                                   16, 1024),
+                    tc::mma_ss(d_tmem, dq + (uint64_t)(((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4),
+                               dk + (uint64_t)(((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4),
                                kIdescQK, kk > 0);
-                tc::commit(&bar[B_SFULL + 2 * t + b]);
+                tc::commit(&bar[B_SFULL + t]);
                 return true;
             };
             // Both tiles' scores for key tile j of this unit (K from its stage).
@@ -474,33 +472,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       (nblk_k - 1) / kBlocksPerTile == nmax - 1;
                 ok = mbar_wait(&bar[B_QFULL], qc & 1);
                 if (ok) ok = issue_s_tile(u, 0);
-                if (ok && nmax > 1) ok = issue_s_tile(u, 1);
                 for (int j = 0; j < nmax && ok; ++j) {
                     const int idx = kvc + j;
                     const int st = idx % kStages;
+                    const int st1 = (idx + 1) % kStages;
+                    // A stage is refilled only after its tile was consumed, so
+                    // per-stage barriers never run two phases ahead.
                     ok = (fix_tail && j == nmax - 1)
-                             ? mbar_wait(&bar[B_VFIXED], (fixc++) & 1)
+                             ? mbar_wait(&bar[B_VFIXED + st], (st ? fixc1++ : fixc0++) & 1)
                              : mbar_wait(&bar[B_VFULL + st], (idx / kStages) & 1);
                     tc::fence_after();
-                    const uint32_t v_base = smem_u32(smem + L::kV + st * L::kKVTile);
+                    const uint64_t dv = dv0 + (uint64_t)((st * L::kKVTile) >> 4);
+                    bool k_next = false;  // K of tile j+1 waited for
+                    // Tile 0's P.V then its next scores, then tile 1's: each
+                    // softmax warpgroup works while the tensor core runs the
+                    // other tile's MMAs.
+                    const int t_last = j < u.ps.n[1] ? 1 : 0;  // last tile to read V_j
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         if (!ok || j >= u.ps.n[t]) continue;
-                        const int G = gt[t] + j, b = G & 1;
-                        ok = mbar_wait(&bar[B_PREADY + 2 * t + b], (G >> 1) & 1);
+                        const int G = gt[t] + j;
+                        ok = mbar_wait(&bar[B_PREADY + t], G & 1);
                         if (ok && j == 0 && units_t[t] > 0)
                             ok = mbar_wait(&bar[B_OFREE + t], (units_t[t] - 1) & 1);
                         tc::fence_after();
                         if (!ok) continue;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk)
-                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t, b) + kk * 8,
-                                       tc::smem_desc_sw128(v_base + kk * 16 * 128, L::kKVHalf, 1024),
-                                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                        tc::commit(&bar[B_ODONE + 2 * t + b]);
+                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t) + kk * 8,
+                                       dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                        tc::commit(&bar[B_ODONE + t]);
+                        if (t == t_last) tc::commit(&bar[B_VEMPTY + st]);  // V_j free
+                        if (j + 1 < u.ps.n[t]) {
+                            if (!k_next) {
+                                ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kStages) & 1);
+                                k_next = true;
+                            }
+                            if (ok) ok = issue_s(t, G + 1, st1);
+                        }
                     }
-                    tc::commit(&bar[B_VEMPTY + st]);
-                    if (ok && j + 2 < nmax) ok = issue_s_tile(u, j + 2);
+                    if (!ok) break;
+                    if (k_next) tc::commit(&bar[B_KEMPTY + st1]);
                 }
                 kvc += nmax;
                 tc::commit(&bar[B_QEMPTY]);  // completes once every MMA of this unit has
@@ -526,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = a.scale_log2;
         bool ok = true;
         int g = 0;  // score tiles of this query tile in earlier units
+        const uint32_t s_tmem = tmem + lane_base + s_col(t);
         for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix)) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
@@ -533,23 +547,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key_lim = min(first_row + r, u.si.k_len - 1);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                const int G = g + j, b = G & 1;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bar[B_SFULL + 2 * t + b], (G >> 1) & 1));
+                const int G = g + j;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], G & 1));
                 if (!ok) break;
                 tc::fence_after();
-                const uint32_t s_tmem = tmem + lane_base + s_col(t, b);
-                uint32_t sr[2][32];
-                tc::ld32(s_tmem, sr[0]);
-                tc::ld32(s_tmem + 32, sr[1]);
-                float mx = -INFINITY;
                 const bool masked = j * kBN + kBN - 1 > first_row;
+                const int kl = key_lim - j * kBN;  // last visible column of this tile
+                // pass 1: row maximum, two 32-column loads per wait
+                float mx = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t sa[32], sb[32];
+                    tc::ld32_issue(s_tmem + c * 32, sa);
+                    tc::ld32_issue(s_tmem + c * 32 + 32, sb);
+                    tc::wait_ld(sa, sb);
+                    if (!masked) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(u2f(sa[i]), u2f(sb[i])));
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        if (masked && j * kBN + c * 32 + i > key_lim) sr[c][i] = f2u(-INFINITY);
-                        mx = fmaxf(mx, u2f(sr[c][i]));
+                        for (int i = 0; i < 32; ++i) {
+                            if (c * 32 + i <= kl) mx = fmaxf(mx, u2f(sa[i]));
+                            if (c * 32 + 32 + i <= kl) mx = fmaxf(mx, u2f(sb[i]));
+                        }
                     }
                 }
                 const float m_tile = mx * sl2;
@@ -561,10 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used = m_tile;
                 }
                 if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                    // O_t must hold the previous tile's P.V before it is scaled.
-                    const int Gp = G - 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + 2 * t + (Gp & 1)],
-                                                           (Gp >> 1) & 1));
+                    // O_t must hold the previous tile's P.V before it is scaled
+                    // (normally complete: S_t itself waited for it).
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], (G - 1) & 1));
                     if (!ok) break;
                     tc::fence_after();
 #pragma unroll
@@ -576,27 +595,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::st32(o_tmem + c * 32, orr);
                     }
                 }
+                // pass 2: P = 2^(s*scale*log2e - m) as fp16, written over S; the
+                // row sum adds the fp32 values before rounding.
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t sa[32], sb[32];
+                    tc::ld32_issue(s_tmem + c * 32, sa);
+                    tc::ld32_issue(s_tmem + c * 32 + 32, sb);
+                    tc::wait_ld(sa, sb);
+                    if (masked) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t pk[16];
+                        for (int i = 0; i < 32; ++i) {
+                            if (c * 32 + i > kl) sa[i] = f2u(-INFINITY);
+                            if (c * 32 + 32 + i > kl) sb[i] = f2u(-INFINITY);
+                        }
+                    }
+                    uint32_t pa[16], pb[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(u2f(sr[c][2 * i]), sl2, -m_used));
-                        const float p1 = ex2(fmaf(u2f(sr[c][2 * i + 1]), sl2, -m_used));
-                        const __half2 hp = __floats2half2_rn(p0, p1);
-                        l += __low2float(hp) + __high2float(hp);
-                        pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                        const float a0 = ex2(fmaf(u2f(sa[2 * i]), sl2, -m_used));
+                        const float a1 = ex2(fmaf(u2f(sa[2 * i + 1]), sl2, -m_used));
+                        const float b0 = ex2(fmaf(u2f(sb[2 * i]), sl2, -m_used));
+                        const float b1 = ex2(fmaf(u2f(sb[2 * i + 1]), sl2, -m_used));
+                        l += (a0 + a1) + (b0 + b1);
+                        const __half2 ha = __floats2half2_rn(a0, a1);
+                        const __half2 hb = __floats2half2_rn(b0, b1);
+                        pa[i] = *reinterpret_cast<const uint32_t *>(&ha);
+                        pb[i] = *reinterpret_cast<const uint32_t *>(&hb);
                     }
-                    tc::st16(s_tmem + c * 16, pk);
+                    tc::st16(s_tmem + c * 16, pa);
+                    tc::st16(s_tmem + c * 16 + 16, pb);
                 }
                 tc::wait_st();
                 tc::fence_before();
-                mbar_arrive(&bar[B_PREADY + 2 * t + b]);
+                mbar_arrive(&bar[B_PREADY + t]);
             }
             if (!ok) break;
             const int Gl = g + n - 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bar[B_ODONE + 2 * t + (Gl & 1)], (Gl >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], Gl & 1));
             if (!ok) break;
             tc::fence_after();
             const bool row_valid = r < u.ps.rows(t);
