@@ -12,18 +12,19 @@
 // (8 cache blocks) past a tile's last row are never loaded, and only the
 // tiles that reach past a tile's first row are masked.
 //
-// Schedule: units are ordered (sequence, head, row pair) and cut into equal
-// contiguous ranges of cost (key tiles to process), one per CTA of a
-// persistent grid, so the CTAs finish together and the units of one
-// (sequence, KV head) run back to back on one SM while their K/V is in L2.
+// Schedule: units are ordered (sequence, head, row pair) and dealt round
+// robin to the CTAs of a persistent grid, so the CTAs running at any moment
+// work on neighbouring units, mostly of the same heads, and read each K/V
+// tile from L2 rather than each from HBM.
 //
 // Roles (384 threads):
 //   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
 //   warps 4-7   softmax of query tile 1
 //   warp 8      producer of the two Q tiles and the K tiles, warp 10 of the
 //               V tiles: TMA loads of one 16-token block x 64-column half
-//               at a time, gathered through the block table into 2-stage
-//               rings, each refilled as soon as its own slot is free
+//               at a time, gathered through the block table into rings (K:
+//               2 stages, V: 3 when shared memory allows, else 2), each
+//               refilled as soon as its own slot is free
 //   warp 9      MMA issuer (one thread) and TMEM owner
 //   warp 11     idle
 // Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
@@ -54,7 +55,7 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kBlocksPerTile = kBN / kBlockSize;
 constexpr int kUnitRows = 2 * kBM;
-constexpr int kStages = 2;  // K/V ring
+constexpr int kKStages = 2;  // K ring; the V ring has VS = 2 or 3 stages
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;
@@ -73,16 +74,16 @@ struct PrefillArgs {
     int B, H, g, maxb, num_blocks, plane_k, plane_v, max_seqlen_q, total_q;
 };
 
-template <int D>
+template <int D, int VS>
 struct PL {
     static constexpr int kQHalf = kBM * 128;          // one 64-column half of a Q tile
     static constexpr int kQTile = kQHalf * (D / 64);
     static constexpr int kKVHalf = kBN * 128;         // one 64-column half of a K/V tile
     static constexpr int kKVTile = kKVHalf * (D / 64);
     static constexpr int kQ = 0;                      // 2 query tiles
-    static constexpr int kK = 2 * kQTile;             // kStages stages
-    static constexpr int kV = kK + kStages * kKVTile;
-    static constexpr int kBar = kV + kStages * kKVTile;
+    static constexpr int kK = 2 * kQTile;             // kKStages stages
+    static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
+    static constexpr int kBar = kV + VS * kKVTile;
     static constexpr int kPrefix = kBar + 512;        // int64 [B + 1]
     static size_t bytes(int B) { return (size_t)kPrefix + (size_t)(B + 1) * 8; }
     static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
@@ -94,17 +95,17 @@ __device__ __forceinline__ uint32_t s_col(int t) { return (uint32_t)(t * kBN); }
 enum {
     B_QFULL = 0,
     B_QEMPTY = 1,
-    B_KFULL = 2,    // kStages
-    B_KEMPTY = 4,   // kStages
-    B_VFULL = 6,    // kStages
-    B_VEMPTY = 8,   // kStages
-    B_VFIXED = 10,  // kStages: a V tile whose tail rows were cleared
-    B_SFULL = 12,   // per query tile
-    B_PREADY = 14,  // per query tile
-    B_ODONE = 16,   // per query tile
-    B_OFREE = 18,   // per query tile
-    B_DRAIN = 20,
-    B_COUNT = 21
+    B_KFULL = 2,    // kKStages
+    B_KEMPTY = 4,   // kKStages
+    B_VFULL = 6,    // up to 3 V stages
+    B_VEMPTY = 9,   // up to 3
+    B_VFIXED = 12,  // up to 3: a V tile whose tail rows were cleared
+    B_SFULL = 15,   // per query tile
+    B_PREADY = 17,  // per query tile
+    B_ODONE = 19,   // per query tile
+    B_OFREE = 21,   // per query tile
+    B_DRAIN = 23,
+    B_COUNT = 24
 };
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -156,90 +157,49 @@ __device__ __forceinline__ bool seq_ok(const PrefillArgs &a, const SeqInfo &si) 
            si.q_begin >= 0 && si.q_begin + si.L_q <= a.total_q;
 }
 
-// Walks the units (s, h, k) of one CTA's cost range in order.
+// The units (s, h, k) of one CTA: unit indices blockIdx.x, blockIdx.x + G,
+// ... of the list ordered (sequence, head, row pair), so the CTAs running at
+// any moment work on neighbouring units, mostly of the same heads, and share
+// those heads' K/V tiles in L2.
 struct UnitIter {
+    int64_t u;      // unit index
     int s, h, k;
-    int64_t start;  // cost offset of the current unit
     SeqInfo si;
     int p, npairs;
     PairShape ps;
 
-    __device__ __forceinline__ void load_seq(const PrefillArgs &a) {
-        si = seq_info(a, s);
-        p = si.k_len - si.L_q;
-        npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
-    }
-    // Move to the first sequence at or after s that has any cost.
-    __device__ __forceinline__ void skip_empty(const PrefillArgs &a, const int64_t *prefix) {
-        while (s < a.B && prefix[s + 1] == prefix[s]) ++s;
-        if (s < a.B) {
-            load_seq(a);
-            ps = pair_shape(p, si.L_q, k);
-        }
-    }
-    // First unit whose start is >= x.
-    __device__ __forceinline__ void init(const PrefillArgs &a, const int64_t *prefix, int64_t x) {
-        const int64_t C = prefix[a.B];
-        h = 0;
-        k = 0;
-        if (x >= C) {
-            s = a.B;
-            start = C;
-            return;
-        }
-        int lo = 0, hi = a.B - 1;  // largest s with prefix[s] <= x
+    // prefix[s] = units of sequences before s (all heads, row pairs)
+    __device__ __forceinline__ void set(const PrefillArgs &a, const int64_t *prefix, int64_t idx) {
+        u = idx;
+        if (u >= prefix[a.B]) return;
+        int lo = 0, hi = a.B - 1;  // largest s with prefix[s] <= u
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= x)
+            if (prefix[mid] <= u)
                 lo = mid;
             else
                 hi = mid - 1;
         }
         s = lo;
-        load_seq(a);
-        const int64_t hc = (prefix[s + 1] - prefix[s]) / a.H;
-        const int64_t off = x - prefix[s];
-        h = (int)(off / hc);
-        const int64_t rem = off - (int64_t)h * hc;
-        int64_t acc = 0;
-        while (acc < rem) {
-            const PairShape q = pair_shape(p, si.L_q, k);
-            acc += q.n[0] + q.n[1];
-            ++k;
-        }
-        start = prefix[s] + (int64_t)h * hc + acc;
-        if (k == npairs) {
-            k = 0;
-            if (++h == a.H) {
-                h = 0;
-                ++s;
-                skip_empty(a, prefix);
-                return;
-            }
-        }
+        si = seq_info(a, s);
+        p = si.k_len - si.L_q;
+        npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
+        const int rem = (int)(u - prefix[s]);
+        h = rem / npairs;
+        k = rem - h * npairs;
         ps = pair_shape(p, si.L_q, k);
     }
     __device__ __forceinline__ void next(const PrefillArgs &a, const int64_t *prefix) {
-        start += ps.n[0] + ps.n[1];
-        if (++k == npairs) {
-            k = 0;
-            if (++h == a.H) {
-                h = 0;
-                ++s;
-                skip_empty(a, prefix);
-                return;
-            }
-        }
-        ps = pair_shape(p, si.L_q, k);
+        set(a, prefix, u + gridDim.x);
     }
-    __device__ __forceinline__ bool valid(int B, int64_t end) const { return s < B && start < end; }
+    __device__ __forceinline__ bool valid(const int64_t *prefix, int B) const { return u < prefix[B]; }
 };
 
-template <int D>
+template <int D, int VS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kvmap, const PrefillArgs a) {
-    using L = PL<D>;
+    using L = PL<D, VS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -250,22 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
 
-    // ---- cost of every sequence (all heads) and its prefix sum
+    // ---- units of every sequence (all heads) and their prefix sum
     for (int s = tid; s < B; s += kThreads) {
         const SeqInfo si = seq_info(a, s);
         int64_t c = 0;
         if (seq_ok(a, si)) {
-            const int p = si.k_len - si.L_q;
-            const int np = (si.L_q + kUnitRows - 1) / kUnitRows;
-            for (int k = 0; k < np; ++k) {
-                const PairShape ps = pair_shape(p, si.L_q, k);
-                c += ps.n[0] + ps.n[1];
-            }
+            c = (int64_t)((si.L_q + kUnitRows - 1) / kUnitRows) * a.H;
             if (si.L_q > a.max_seqlen_q && blockIdx.x == 0) report(a.status, PA_DEV_BAD_LENGTH);
         } else if (blockIdx.x == 0) {
             report(a.status, PA_DEV_BAD_LENGTH);
         }
-        prefix[s + 1] = c * a.H;
+        prefix[s + 1] = c;
     }
     if (tid == 0) prefix[0] = 0;
     __syncthreads();
@@ -284,19 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    const int64_t C = prefix[B];
-    const int G = gridDim.x;
-    const int64_t range_lo = C * blockIdx.x / G, range_hi = C * (blockIdx.x + 1) / G;
     UnitIter first;
-    first.init(a, prefix, range_lo);
-    if (!first.valid(B, range_hi)) return;  // no unit starts in this range (whole CTA)
+    first.set(a, prefix, blockIdx.x);
+    if (!first.valid(prefix, B)) return;  // no unit for this CTA (whole CTA)
 
     if (tid == 0) {
         mbar_init(&bar[B_QFULL], 1);
         mbar_init(&bar[B_QEMPTY], 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&bar[B_KFULL + i], 1);
             mbar_init(&bar[B_KEMPTY + i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
             mbar_init(&bar[B_VFULL + i], 1);
             mbar_init(&bar[B_VEMPTY + i], 1);
             mbar_init(&bar[B_VFIXED + i], 1);
@@ -327,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool is_v = warp == kVProducerWarp;
         const int full0 = is_v ? B_VFULL : B_KFULL;
         const int empty0 = is_v ? B_VEMPTY : B_KEMPTY;
+        const int nst = is_v ? VS : kKStages;  // ring depth
         const int plane = is_v ? a.plane_v : a.plane_k;
         uint8_t *const ring = smem + (is_v ? L::kV : L::kK);
         int ok = 1;
@@ -335,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&kvmap);
         }
         int kvc = 0, qc = 0;
-        for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix), ++qc) {
+        for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix), ++qc) {
             const int nmax = max(u.ps.n[0], u.ps.n[1]);
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
@@ -369,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nmax && ok; ++j) {
                 const int rows_next = j + 1 < nmax ? block_row(j + 1) : 0;
                 const int idx = kvc + j;
-                const int st = idx % kStages;
-                const uint32_t ph = (idx / kStages) & 1;
+                const int st = idx % nst;
+                const uint32_t ph = (idx / nst) & 1;
                 int rr[kBlocksPerTile];
 #pragma unroll
                 for (int b = 0; b < kBlocksPerTile; ++b)
@@ -419,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             // Leave no copy in flight: the last tiles' loads have landed.
-            for (int i = max(0, kvc - kStages); i < kvc; ++i)
-                mbar_wait(&bar[full0 + i % kStages], (i / kStages) & 1);
+            for (int i = max(0, kvc - nst); i < kvc; ++i)
+                mbar_wait(&bar[full0 + i % nst], (i / nst) & 1);
             if (!is_v && qc > 0) mbar_wait(&bar[B_QFULL], (qc - 1) & 1);
         }
       } else if (warp == kMmaWarp) {
@@ -430,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
             bool ok = true;
             int kvc = 0, qc = 0;
-            int fixc0 = 0, fixc1 = 0;  // cleared V tiles of ring stage 0 / 1
+            int fixc0 = 0, fixc1 = 0, fixc2 = 0;  // cleared V tiles per V stage
             int gt[2] = {0, 0};       // score tiles of query tile t in earlier units
             int units_t[2] = {0, 0};  // earlier units with a non-empty tile t
             // Shared-memory descriptors of every operand buffer, built once; a
@@ -457,15 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Both tiles' scores for key tile j of this unit (K from its stage).
             auto issue_s_tile = [&](const UnitIter &u, int j) -> bool {
                 const int idx = kvc + j;
-                const int st = idx % kStages;
-                if (!mbar_wait(&bar[B_KFULL + st], (idx / kStages) & 1)) return false;
+                const int st = idx % kKStages;
+                if (!mbar_wait(&bar[B_KFULL + st], (idx / kKStages) & 1)) return false;
                 tc::fence_after();
                 if (j < u.ps.n[0] && !issue_s(0, gt[0] + j, st)) return false;
                 if (j < u.ps.n[1] && !issue_s(1, gt[1] + j, st)) return false;
                 tc::commit(&bar[B_KEMPTY + st]);
                 return true;
             };
-            for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix), ++qc) {
+            for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix), ++qc) {
                 const int nmax = max(u.ps.n[0], u.ps.n[1]);
                 const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                 const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
@@ -474,13 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ok = issue_s_tile(u, 0);
                 for (int j = 0; j < nmax && ok; ++j) {
                     const int idx = kvc + j;
-                    const int st = idx % kStages;
-                    const int st1 = (idx + 1) % kStages;
+                    const int st = idx % VS;               // V stage of tile j
+                    const int st1 = (idx + 1) % kKStages;  // K stage of tile j+1
                     // A stage is refilled only after its tile was consumed, so
                     // per-stage barriers never run two phases ahead.
                     ok = (fix_tail && j == nmax - 1)
-                             ? mbar_wait(&bar[B_VFIXED + st], (st ? fixc1++ : fixc0++) & 1)
-                             : mbar_wait(&bar[B_VFULL + st], (idx / kStages) & 1);
+                             ? mbar_wait(&bar[B_VFIXED + st],
+                                         (st == 0 ? fixc0++ : st == 1 ? fixc1++ : fixc2++) & 1)
+                             : mbar_wait(&bar[B_VFULL + st], (idx / VS) & 1);
                     tc::fence_after();
                     const uint64_t dv = dv0 + (uint64_t)((st * L::kKVTile) >> 4);
                     bool k_next = false;  // K of tile j+1 waited for
@@ -506,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (t == t_last) tc::commit(&bar[B_VEMPTY + st]);  // V_j free
                         if (j + 1 < u.ps.n[t]) {
                             if (!k_next) {
-                                ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kStages) & 1);
+                                ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kKStages) & 1);
                                 k_next = true;
                             }
                             if (ok) ok = issue_s(t, G + 1, st1);
@@ -540,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g = 0;  // score tiles of this query tile in earlier units
         const uint32_t s_tmem = tmem + lane_base + s_col(t);
-        for (UnitIter u = first; u.valid(B, range_hi) && ok; u.next(a, prefix)) {
+        for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix)) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
             const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
@@ -684,23 +640,29 @@ bool make_rows_map(CUtensorMap *map, const void *base, int T, int H, int D) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
-                   cudaStream_t st) {
+constexpr size_t kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per CTA
+
+template <int D, int VS>
+size_t prefill_smem(int B) {
+    // At least 116 KB keeps one CTA per SM, so no CTA waits in tcgen05.alloc
+    // for another's 512 TMEM columns.
+    const size_t need = PL<D, VS>::bytes(B) + 1024;
+    return need > 116 * 1024 ? need : 116 * 1024;
+}
+
+template <int D, int VS>
+int launch_prefill_vs(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
+                      cudaStream_t st) {
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-    // At least 116 KB of shared memory keeps one CTA per SM, so no CTA waits
-    // in tcgen05.alloc for another's 512 TMEM columns.
-    const size_t smax = PL<D>::bytes(kMaxSeqs) + 1024;
-    const size_t need = PL<D>::bytes(a.B) + 1024;
-    const size_t smem = need > 116 * 1024 ? need : 116 * 1024;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(smax > 116 * 1024 ? smax : 116 * 1024)) != cudaSuccess) {
+            if (cudaFuncSetAttribute(prefill_kernel<D, VS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemLimit) != cudaSuccess) {
                 cudaGetLastError();
                 return PA_ERR_CUDA;
             }
@@ -709,8 +671,18 @@ int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const Pref
     }
     const int grid = sm_count();
     if (grid < 1) return PA_ERR_CUDA;
-    prefill_kernel<D><<<grid, kThreads, smem, st>>>(qmap, kvmap, a);
+    prefill_kernel<D, VS><<<grid, kThreads, prefill_smem<D, VS>(a.B), st>>>(qmap, kvmap, a);
     return launch_status();
+}
+
+// Three V stages when the batch's prefix table leaves room for them (they
+// hide the ~3 us a paged V tile takes to arrive); two otherwise.
+template <int D>
+int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
+                   cudaStream_t st) {
+    if (prefill_smem<D, 3>(a.B) <= kSmemLimit) return launch_prefill_vs<D, 3>(qmap, kvmap, a, st);
+    if (prefill_smem<D, 2>(a.B) <= kSmemLimit) return launch_prefill_vs<D, 2>(qmap, kvmap, a, st);
+    return PA_ERR_UNSUPPORTED;
 }
 
 }  // namespace

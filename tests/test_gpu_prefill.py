@@ -173,3 +173,14 @@ def test_prefill_bad_lengths_are_reported():
     pa.prefill_varlen(run.q, run.cache, run.cuq, bad, run.bt, 20, 2, status=run.status)
     torch.cuda.synchronize()
     assert int(run.status.item()) & pa.PA_DEV_BAD_LENGTH
+
+
+def test_prefill_many_sequences():
+    """A batch large enough that the kernel keeps two V stages (its
+    per-sequence table takes the third stage's shared memory)."""
+    rng = np.random.default_rng(41)
+    B = 300
+    cached = rng.integers(0, 60, size=B).tolist()
+    new = rng.integers(1, 40, size=B).tolist()
+    case, init = custom_prefill_case(4, 2, 128, cached, new, seed=42)
+    check(case, init)
