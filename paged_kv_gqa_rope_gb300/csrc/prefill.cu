@@ -30,7 +30,9 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
 // tile, head_dim per O).  Per key tile j the MMA thread issues, in order,
 //   O0 += P0 . V_j   (A = P0 from TMEM, once softmax_0 wrote it over S0)
-//   S0  = Q0 . K_j+1^T (after that P.V has completed: same TMEM)
+//   S0  = Q0 . K_j+1^T (same TMEM as P0: tcgen05.mma operations issued by
+//                       one thread execute in issue order, so the P.V has
+//                       read P0 before S0 is written; no wait in between)
 //   O1 += P1 . V_j,  S1 = Q1 . K_j+1^T
 // so softmax_0 works on S0(j+1) while the tensor core runs tile 1's MMAs and
 // softmax_1 while it runs tile 0's.  Every MMA has N = 128 (M = 128, K = 16):
@@ -84,8 +86,8 @@ struct PL {
     static constexpr int kK = 2 * kQTile;             // kKStages stages
     static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
     static constexpr int kBar = kV + VS * kKVTile;
-    static constexpr int kPrefix = kBar + 512;        // int64 [B + 1]
-    static size_t bytes(int B) { return (size_t)kPrefix + (size_t)(B + 1) * 8; }
+    static constexpr int kTab = kBar + 512;           // int4 [B + 1]: sequence table
+    static size_t bytes(int B) { return (size_t)kTab + (size_t)(B + 1) * 16; }
     static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
 };
 
@@ -160,39 +162,41 @@ __device__ __forceinline__ bool seq_ok(const PrefillArgs &a, const SeqInfo &si) 
 // The units (s, h, k) of one CTA: unit indices blockIdx.x, blockIdx.x + G,
 // ... of the list ordered (sequence, head, row pair), so the CTAs running at
 // any moment work on neighbouring units, mostly of the same heads, and share
-// those heads' K/V tiles in L2.
+// those heads' K/V tiles in L2.  `tab` is the shared-memory sequence table:
+// tab[s] = {units of sequences before s, q_begin, L_q, k_len}, tab[B].x =
+// all units.
 struct UnitIter {
-    int64_t u;      // unit index
+    int u;  // unit index
     int s, h, k;
     SeqInfo si;
     int p, npairs;
     PairShape ps;
 
-    // prefix[s] = units of sequences before s (all heads, row pairs)
-    __device__ __forceinline__ void set(const PrefillArgs &a, const int64_t *prefix, int64_t idx) {
+    __device__ __forceinline__ void set(int B, const int4 *tab, int idx) {
         u = idx;
-        if (u >= prefix[a.B]) return;
-        int lo = 0, hi = a.B - 1;  // largest s with prefix[s] <= u
+        if (u >= tab[B].x) return;
+        int lo = 0, hi = B - 1;  // largest s with tab[s].x <= u
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= u)
+            if (tab[mid].x <= u)
                 lo = mid;
             else
                 hi = mid - 1;
         }
         s = lo;
-        si = seq_info(a, s);
+        const int4 e = tab[s];
+        si.q_begin = e.y;
+        si.L_q = e.z;
+        si.k_len = e.w;
         p = si.k_len - si.L_q;
         npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
-        const int rem = (int)(u - prefix[s]);
+        const int rem = u - e.x;
         h = rem / npairs;
         k = rem - h * npairs;
         ps = pair_shape(p, si.L_q, k);
     }
-    __device__ __forceinline__ void next(const PrefillArgs &a, const int64_t *prefix) {
-        set(a, prefix, u + gridDim.x);
-    }
-    __device__ __forceinline__ bool valid(const int64_t *prefix, int B) const { return u < prefix[B]; }
+    __device__ __forceinline__ void next(int B, const int4 *tab) { set(B, tab, u + gridDim.x); }
+    __device__ __forceinline__ bool valid(int B, const int4 *tab) const { return u < tab[B].x; }
 };
 
 template <int D, int VS>
@@ -205,43 +209,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
-    int64_t *prefix = reinterpret_cast<int64_t *>(smem + L::kPrefix);
+    int4 *tab = reinterpret_cast<int4 *>(smem + L::kTab);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
 
-    // ---- units of every sequence (all heads) and their prefix sum
+    // ---- sequence table: lengths and the running count of units
     for (int s = tid; s < B; s += kThreads) {
         const SeqInfo si = seq_info(a, s);
-        int64_t c = 0;
+        int c = 0;
         if (seq_ok(a, si)) {
-            c = (int64_t)((si.L_q + kUnitRows - 1) / kUnitRows) * a.H;
+            c = ((si.L_q + kUnitRows - 1) / kUnitRows) * a.H;
             if (si.L_q > a.max_seqlen_q && blockIdx.x == 0) report(a.status, PA_DEV_BAD_LENGTH);
         } else if (blockIdx.x == 0) {
             report(a.status, PA_DEV_BAD_LENGTH);
         }
-        prefix[s + 1] = c;
+        tab[s].y = si.q_begin;
+        tab[s].z = si.L_q;
+        tab[s].w = si.k_len;
+        tab[s + 1].x = c;  // units of sequence s, summed below
     }
-    if (tid == 0) prefix[0] = 0;
+    if (tid == 0) tab[0].x = 0;
     __syncthreads();
     if (warp == 0) {
-        int64_t carry = 0;
+        int carry = 0;
         for (int base = 1; base <= B; base += 32) {
             const int i = base + lane;
-            int64_t v = i <= B ? prefix[i] : 0;
+            int v = i <= B ? tab[i].x : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int64_t t = __shfl_up_sync(0xffffffffu, v, o);
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += t;
             }
-            if (i <= B) prefix[i] = v + carry;
+            if (i <= B) tab[i].x = v + carry;
             carry += __shfl_sync(0xffffffffu, v, 31);
         }
     }
     __syncthreads();
     UnitIter first;
-    first.set(a, prefix, blockIdx.x);
-    if (!first.valid(prefix, B)) return;  // no unit for this CTA (whole CTA)
+    first.set(B, tab, blockIdx.x);
+    if (!first.valid(B, tab)) return;  // no unit for this CTA (whole CTA)
 
     if (tid == 0) {
         mbar_init(&bar[B_QFULL], 1);
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&kvmap);
         }
         int kvc = 0, qc = 0;
-        for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix), ++qc) {
+        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab), ++qc) {
             const int nmax = max(u.ps.n[0], u.ps.n[1]);
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
@@ -393,10 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
             const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(smem + L::kV), L::kKVHalf, 1024);
-            // S_t for global score tile G, once the P.V of tile G - 1 (which
-            // read the same TMEM) has completed.
-            auto issue_s = [&](int t, int G, int st) -> bool {
-                if (G >= 1 && !mbar_wait(&bar[B_ODONE + t], (G - 1) & 1)) return false;
+            // S_t for global score tile G (its TMEM held P_t of tile G - 1).
+            auto issue_s = [&](int t, int G, int st, bool after_pv) -> bool {
+                // Within a unit, S_t is issued right behind the P_t.V that reads
+                // the same TMEM, by this thread: tcgen05.mma operations issued by
+                // one thread run in issue order, so that P.V has read P before S
+                // is written.  Across units the previous P.V is waited for.
+                if (!after_pv && G >= 1 && !mbar_wait(&bar[B_ODONE + t], (G - 1) & 1))
+                    return false;
                 tc::fence_after();
                 const uint64_t dq = dq0 + (uint64_t)((t * L::kQTile) >> 4);
                 const uint64_t dk = dk0 + (uint64_t)((st * L::kKVTile) >> 4);
@@ -415,12 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = idx % kKStages;
                 if (!mbar_wait(&bar[B_KFULL + st], (idx / kKStages) & 1)) return false;
                 tc::fence_after();
-                if (j < u.ps.n[0] && !issue_s(0, gt[0] + j, st)) return false;
-                if (j < u.ps.n[1] && !issue_s(1, gt[1] + j, st)) return false;
+                if (j < u.ps.n[0] && !issue_s(0, gt[0] + j, st, false)) return false;
+                if (j < u.ps.n[1] && !issue_s(1, gt[1] + j, st, false)) return false;
                 tc::commit(&bar[B_KEMPTY + st]);
                 return true;
             };
-            for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix), ++qc) {
+            for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab), ++qc) {
                 const int nmax = max(u.ps.n[0], u.ps.n[1]);
                 const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                 const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
@@ -465,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kKStages) & 1);
                                 k_next = true;
                             }
-                            if (ok) ok = issue_s(t, G + 1, st1);
+                            if (ok) ok = issue_s(t, G + 1, st1, true);
                         }
                     }
                     if (!ok) break;
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g = 0;  // score tiles of this query tile in earlier units
         const uint32_t s_tmem = tmem + lane_base + s_col(t);
-        for (UnitIter u = first; u.valid(prefix, B) && ok; u.next(a, prefix)) {
+        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
             const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
@@ -538,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (j > 0 && __any_sync(0xffffffffu, raise)) {
                     // O_t must hold the previous tile's P.V before it is scaled
-                    // (normally complete: S_t itself waited for it).
+                    // (normally complete: S_t was issued behind it).
                     ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], (G - 1) & 1));
                     if (!ok) break;
                     tc::fence_after();
