@@ -529,8 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::ld32_issue(s_tmem + c * 32 + 32, sb);
                     tc::wait_ld(sa, sb);
                     if (!masked) {
+                        float m1 = -INFINITY;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(u2f(sa[i]), u2f(sb[i])));
+                        for (int i = 0; i < 32; i += 2) {
+                            mx = fmax3(mx, u2f(sa[i]), u2f(sa[i + 1]));
+                            m1 = fmax3(m1, u2f(sb[i]), u2f(sb[i + 1]));
+                        }
+                        mx = fmaxf(mx, m1);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
@@ -564,6 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // pass 2: P = 2^(s*scale*log2e - m) as fp16, written over S; the
                 // row sum adds the fp32 values before rounding.
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t negm = f2_pack(-m_used, -m_used);
+                uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
 #pragma unroll 1
                 for (int c = 0; c < 4; c += 2) {
                     uint32_t sa[32], sb[32];
@@ -577,21 +585,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c * 32 + 32 + i > kl) sb[i] = f2u(-INFINITY);
                         }
                     }
+                    // Pairs of columns go through one packed fp32 FMA and add.
                     uint32_t pa[16], pb[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float a0 = ex2(fmaf(u2f(sa[2 * i]), sl2, -m_used));
-                        const float a1 = ex2(fmaf(u2f(sa[2 * i + 1]), sl2, -m_used));
-                        const float b0 = ex2(fmaf(u2f(sb[2 * i]), sl2, -m_used));
-                        const float b1 = ex2(fmaf(u2f(sb[2 * i + 1]), sl2, -m_used));
-                        l += (a0 + a1) + (b0 + b1);
-                        const __half2 ha = __floats2half2_rn(a0, a1);
-                        const __half2 hb = __floats2half2_rn(b0, b1);
-                        pa[i] = *reinterpret_cast<const uint32_t *>(&ha);
-                        pb[i] = *reinterpret_cast<const uint32_t *>(&hb);
+                        float a0, a1, b0, b1;
+                        f2_unpack(f2_fma(f2_pack(u2f(sa[2 * i]), u2f(sa[2 * i + 1])), sl2x2, negm),
+                                  a0, a1);
+                        f2_unpack(f2_fma(f2_pack(u2f(sb[2 * i]), u2f(sb[2 * i + 1])), sl2x2, negm),
+                                  b0, b1);
+                        a0 = ex2(a0);
+                        a1 = ex2(a1);
+                        b0 = ex2(b0);
+                        b1 = ex2(b1);
+                        la = f2_add(la, f2_pack(a0, a1));
+                        lb = f2_add(lb, f2_pack(b0, b1));
+                        pa[i] = pack_half2(a0, a1);
+                        pb[i] = pack_half2(b0, b1);
                     }
                     tc::st16(s_tmem + c * 16, pa);
                     tc::st16(s_tmem + c * 16 + 16, pb);
+                }
+                {
+                    float x0, x1, y0, y1;
+                    f2_unpack(la, x0, x1);
+                    f2_unpack(lb, y0, y1);
+                    l += (x0 + x1) + (y0 + y1);
                 }
                 tc::wait_st();
                 tc::fence_before();
