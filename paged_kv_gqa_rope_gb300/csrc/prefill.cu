@@ -95,19 +95,19 @@ struct PL {
 __device__ __forceinline__ uint32_t s_col(int t) { return (uint32_t)(t * kBN); }
 
 enum {
-    B_QFULL = 0,
-    B_QEMPTY = 1,
-    B_KFULL = 2,    // kKStages
-    B_KEMPTY = 4,   // kKStages
-    B_VFULL = 6,    // up to 3 V stages
-    B_VEMPTY = 9,   // up to 3
-    B_VFIXED = 12,  // up to 3: a V tile whose tail rows were cleared
-    B_SFULL = 15,   // per query tile
-    B_PREADY = 17,  // per query tile
-    B_ODONE = 19,   // per query tile
-    B_OFREE = 21,   // per query tile
-    B_DRAIN = 23,
-    B_COUNT = 24
+    B_QFULL = 0,    // per query tile
+    B_QEMPTY = 2,   // per query tile
+    B_KFULL = 4,    // kKStages
+    B_KEMPTY = 6,   // kKStages
+    B_VFULL = 8,    // up to 3 V stages
+    B_VEMPTY = 11,  // up to 3
+    B_VFIXED = 14,  // up to 3: a V tile whose tail rows were cleared
+    B_SFULL = 17,   // per query tile
+    B_PREADY = 19,  // per query tile
+    B_ODONE = 21,   // per query tile
+    B_OFREE = 23,   // per query tile
+    B_DRAIN = 25,
+    B_COUNT = 26
 };
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -251,8 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!first.valid(B, tab)) return;  // no unit for this CTA (whole CTA)
 
     if (tid == 0) {
-        mbar_init(&bar[B_QFULL], 1);
-        mbar_init(&bar[B_QEMPTY], 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&bar[B_KFULL + i], 1);
             mbar_init(&bar[B_KEMPTY + i], 1);
@@ -263,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_VFIXED + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[B_QFULL + i], 1);
+            mbar_init(&bar[B_QEMPTY + i], 1);
             mbar_init(&bar[B_SFULL + i], 1);
             mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_ODONE + i], 1);
@@ -296,40 +296,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!is_v) tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kvmap);
         }
-        int kvc = 0, qc = 0;
-        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab), ++qc) {
+        // Cache row of this lane's block (lanes 0-7) of key tile j of unit u.
+        auto block_row = [&](const UnitIter &u, int j) -> int {
+            const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
+            const int lb = j * kBlocksPerTile + lane;
+            if (lane >= kBlocksPerTile || lb >= nblk_k) return oob_row;
+            const int blk = __ldg(a.block_tables + (int64_t)u.s * a.maxb + lb);
+            if (blk < 0 || blk >= a.num_blocks) {
+                if (!is_v) report(a.status, PA_DEV_BAD_BLOCK);
+                return oob_row;
+            }
+            return blk * kBlockSize;
+        };
+        int kvc = 0, qn0 = 0, qn1 = 0;  // K/V tiles, Q tiles per query tile, loaded so far
+        int rows_cur = block_row(first, 0);
+        for (UnitIter u = first; u.valid(B, tab) && ok;) {
+            UnitIter un = u;  // the next unit: its first block rows are looked up early
+            un.next(B, tab);
             const int nmax = max(u.ps.n[0], u.ps.n[1]);
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
             const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
             const bool fix_tail = is_v && (u.si.k_len % kBlockSize) != 0 &&
                                   (nblk_k - 1) / kBlocksPerTile == nmax - 1;
-            const int32_t *row = a.block_tables + (int64_t)u.s * a.maxb;
-            auto block_row = [&](int j) -> int {  // cache row of this lane's block of tile j
-                const int lb = j * kBlocksPerTile + lane;
-                if (lane >= kBlocksPerTile || lb >= nblk_k) return oob_row;
-                const int blk = __ldg(row + lb);
-                if (blk < 0 || blk >= a.num_blocks) {
-                    if (!is_v) report(a.status, PA_DEV_BAD_BLOCK);
-                    return oob_row;
-                }
-                return blk * kBlockSize;
-            };
-            if (!is_v && lane == 0) {
-                if (qc > 0) ok = mbar_wait(&bar[B_QEMPTY], (qc - 1) & 1);
-                if (ok) {
-                    const int ntiles = u.ps.rv[1] > 0 ? 2 : 1;
-                    mbar_arrive_expect_tx(&bar[B_QFULL], L::kQTile * ntiles);
-                    for (int t = 0; t < ntiles; ++t)
-                        for (int hf = 0; hf < D / 64; ++hf)
-                            tma_load_4d(smem + L::kQ + t * L::kQTile + hf * L::kQHalf, &qmap,
-                                        &bar[B_QFULL], 0, hf, u.h, u.si.q_begin + q0 + t * kBM);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            int rows_cur = block_row(0);
             for (int j = 0; j < nmax && ok; ++j) {
-                const int rows_next = j + 1 < nmax ? block_row(j + 1) : 0;
+                const int rows_next = j + 1 < nmax ? block_row(u, j + 1)
+                                      : un.valid(B, tab) ? block_row(un, 0) : 0;
                 const int idx = kvc + j;
                 const int st = idx % nst;
                 const uint32_t ph = (idx / nst) & 1;
@@ -347,6 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int hf = 0; hf < D / 64; ++hf)
                                 tma_load_5d(dst + hf * L::kKVHalf + b * kBlockSize * 128, &kvmap,
                                             &bar[full0 + st], 0, hf, kvh, rr[b], plane);
+                    }
+                }
+                if (!is_v && j == 0 && lane == 0) {
+                    // Q tiles after K_0: K_0's stage frees earlier than a Q
+                    // buffer, which waits for its tile's last S of the unit before.
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        int &qn = t ? qn1 : qn0;
+                        if (!ok || u.ps.tiles(t) == 0) continue;
+                        if (qn > 0) ok = mbar_wait(&bar[B_QEMPTY + t], (qn - 1) & 1);
+                        if (!ok) continue;
+                        mbar_arrive_expect_tx(&bar[B_QFULL + t], L::kQTile);
+                        for (int hf = 0; hf < D / 64; ++hf)
+                            tma_load_4d(smem + L::kQ + t * L::kQTile + hf * L::kQHalf, &qmap,
+                                        &bar[B_QFULL + t], 0, hf, u.h,
+                                        u.si.q_begin + q0 + t * kBM);
+                        ++qn;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -377,13 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rows_cur = rows_next;
             }
             kvc += nmax;
+            u = un;
         }
         if (lane == 0) {
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             // Leave no copy in flight: the last tiles' loads have landed.
             for (int i = max(0, kvc - nst); i < kvc; ++i)
                 mbar_wait(&bar[full0 + i % nst], (i / nst) & 1);
-            if (!is_v && qc > 0) mbar_wait(&bar[B_QFULL], (qc - 1) & 1);
+            if (!is_v && qn0 > 0) mbar_wait(&bar[B_QFULL], (qn0 - 1) & 1);
+            if (!is_v && qn1 > 0) mbar_wait(&bar[B_QFULL + 1], (qn1 - 1) & 1);
         }
       } else if (warp == kMmaWarp) {
         // ======================= MMA issuer (one thread)
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN, false, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
             bool ok = true;
-            int kvc = 0, qc = 0;
+            int kvc = 0;
             int fixc0 = 0, fixc1 = 0, fixc2 = 0;  // cleared V tiles per V stage
             int gt[2] = {0, 0};       // score tiles of query tile t in earlier units
             int units_t[2] = {0, 0};  // earlier units with a non-empty tile t
@@ -400,15 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
             const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(smem + L::kV), L::kKVHalf, 1024);
-            // S_t for global score tile G (its TMEM held P_t of tile G - 1).
-            auto issue_s = [&](int t, int G, int st, bool after_pv) -> bool {
-                // Within a unit, S_t is issued right behind the P_t.V that reads
-                // the same TMEM, by this thread: tcgen05.mma operations issued by
-                // one thread run in issue order, so that P.V has read P before S
-                // is written.  Across units the previous P.V is waited for.
-                if (!after_pv && G >= 1 && !mbar_wait(&bar[B_ODONE + t], (G - 1) & 1))
-                    return false;
-                tc::fence_after();
+            // S_t for key tile j of unit u, K from ring stage st.  Its TMEM held
+            // P_t of the previous score tile: the P.V that read it was issued
+            // earlier by this thread, and tcgen05.mma operations issued by one
+            // thread run in issue order.  After the unit's last S_t the Q_t
+            // buffer is released to the next unit.
+            auto issue_s = [&](const UnitIter &u, int t, int j, int st) {
                 const uint64_t dq = dq0 + (uint64_t)((t * L::kQTile) >> 4);
                 const uint64_t dk = dk0 + (uint64_t)((st * L::kKVTile) >> 4);
                 const uint32_t d_tmem = tmem + s_col(t);
@@ -418,26 +426,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                dk + (uint64_t)(((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4),
                                kIdescQK, kk > 0);
                 tc::commit(&bar[B_SFULL + t]);
-                return true;
+                if (j + 1 == u.ps.tiles(t)) tc::commit(&bar[B_QEMPTY + t]);
             };
             // Both tiles' scores for key tile j of this unit (K from its stage).
             auto issue_s_tile = [&](const UnitIter &u, int j) -> bool {
                 const int idx = kvc + j;
                 const int st = idx % kKStages;
                 if (!mbar_wait(&bar[B_KFULL + st], (idx / kKStages) & 1)) return false;
-                tc::fence_after();
-                if (j < u.ps.n[0] && !issue_s(0, gt[0] + j, st, false)) return false;
-                if (j < u.ps.n[1] && !issue_s(1, gt[1] + j, st, false)) return false;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= u.ps.tiles(t)) continue;
+                    if (!mbar_wait(&bar[B_QFULL + t], (t ? units_t[1] : units_t[0]) & 1)) return false;
+                    tc::fence_after();
+                    issue_s(u, t, j, st);
+                }
                 tc::commit(&bar[B_KEMPTY + st]);
                 return true;
             };
-            for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab), ++qc) {
+            for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
                 const int nmax = max(u.ps.n[0], u.ps.n[1]);
                 const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                 const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
                                       (nblk_k - 1) / kBlocksPerTile == nmax - 1;
-                ok = mbar_wait(&bar[B_QFULL], qc & 1);
-                if (ok) ok = issue_s_tile(u, 0);
+                ok = issue_s_tile(u, 0);
                 for (int j = 0; j < nmax && ok; ++j) {
                     const int idx = kvc + j;
                     const int st = idx % VS;               // V stage of tile j
@@ -474,16 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j + 1 < u.ps.n[t]) {
                             if (!k_next) {
                                 ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kKStages) & 1);
+                                tc::fence_after();
                                 k_next = true;
                             }
-                            if (ok) ok = issue_s(t, G + 1, st1, true);
+                            if (ok) issue_s(u, t, j + 1, st1);
                         }
                     }
                     if (!ok) break;
                     if (k_next) tc::commit(&bar[B_KEMPTY + st1]);
                 }
                 kvc += nmax;
-                tc::commit(&bar[B_QEMPTY]);  // completes once every MMA of this unit has
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     gt[t] += u.ps.n[t];
