@@ -17,7 +17,7 @@
 // work on neighbouring units, mostly of the same heads, and read each K/V
 // tile from L2 rather than each from HBM.
 //
-// Roles (384 threads):
+// Roles (512 threads):
 //   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
 //   warps 4-7   softmax of query tile 1
 //   warp 8      producer of the two Q tiles and the K tiles, warp 10 of the
@@ -27,6 +27,8 @@
 //               refilled as soon as its own slot is free
 //   warp 9      MMA issuer (one thread) and TMEM owner
 //   warp 11     idle
+//   warps 12-15 output: O_t / l of a finished tile to global memory, while
+//               the softmax warpgroups already work on the next unit
 // Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
 // tile, head_dim per O).  Per key tile j the MMA thread issues, in order,
 //   O0 += P0 . V_j   (A = P0 from TMEM, once softmax_0 wrote it over S0)
@@ -61,7 +63,8 @@ constexpr int kKStages = 2;  // K ring; the V ring has VS = 2 or 3 stages
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;
-constexpr int kThreads = 12 * 32;  // 168 registers per thread, no spills
+constexpr int kEpilogueWarp = 12;  // warps 12-15
+constexpr int kThreads = 16 * 32;  // 128 registers per thread, no spills
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSeqs = 2048;
@@ -86,7 +89,8 @@ struct PL {
     static constexpr int kK = 2 * kQTile;             // kKStages stages
     static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
     static constexpr int kBar = kV + VS * kKVTile;
-    static constexpr int kTab = kBar + 512;           // int4 [B + 1]: sequence table
+    static constexpr int kLsum = kBar + 512;          // float [2 tiles][2 units][128]: row sums
+    static constexpr int kTab = kLsum + 2048;         // int4 [B + 1]: sequence table
     static size_t bytes(int B) { return (size_t)kTab + (size_t)(B + 1) * 16; }
     static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
 };
@@ -107,7 +111,8 @@ enum {
     B_ODONE = 21,   // per query tile
     B_OFREE = 23,   // per query tile
     B_DRAIN = 25,
-    B_COUNT = 26
+    B_LREADY = 26,  // per query tile and unit parity: row sums written
+    B_COUNT = 30
 };
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -267,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_ODONE + i], 1);
             mbar_init(&bar[B_OFREE + i], 128);
+            mbar_init(&bar[B_LREADY + 2 * i], 128);
+            mbar_init(&bar[B_LREADY + 2 * i + 1], 128);
         }
         mbar_init(&bar[B_DRAIN], 1);
         fence_barrier_init();
@@ -281,7 +288,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
-    if (warp >= kProducerWarp) {
+    float *lsum = reinterpret_cast<float *>(smem + L::kLsum);
+
+    if (warp >= kEpilogueWarp) {
+        // ======================= output warpgroup: thread = query row of the
+        // finished tile.  It reads O_t once the unit's last P.V completed,
+        // releases O_t to the next unit and stores O_t / l; the softmax
+        // warpgroups meanwhile work on the next unit.
+        const int r = tid - kEpilogueWarp * 32;  // TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        bool ok = true;
+        int g0 = 0, g1 = 0;    // score tiles of query tile 0 / 1 in earlier units
+        int un0 = 0, un1 = 0;  // earlier units with rows in query tile 0 / 1
+        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int n = u.ps.tiles(t);
+                int &g = t ? g1 : g0;
+                int &un = t ? un1 : un0;
+                if (!ok || n == 0) continue;
+                const int slot = 2 * t + (un & 1);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bar[B_LREADY + slot], (un >> 1) & 1) &&
+                                    mbar_wait(&bar[B_ODONE + t], (g + n - 1) & 1));
+                if (!ok) continue;
+                tc::fence_after();
+                const float l = lsum[slot * 128 + r];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint32_t h[D / 2];  // O / l as fp16 pairs
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tc::ld32(tmem + lane_base + L::kOCol + t * D + c * 32, orr);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[c * 16 + i] = pack_half2(u2f(orr[2 * i]) * inv, u2f(orr[2 * i + 1]) * inv);
+                }
+                tc::fence_before();
+                mbar_arrive(&bar[B_OFREE + t]);  // O_t read: the next unit may overwrite it
+                if (r < u.ps.rows(t)) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        a.out +
+                        ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
+#pragma unroll
+                    for (int v = 0; v < D / 8; ++v)
+                        dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                }
+                g += n;
+                ++un;
+            }
+        }
+        if (!ok && lane == 0) report(a.status, PA_DEV_TIMEOUT);
+    } else if (warp >= kProducerWarp) {
       if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ======================= producers: Q and K tiles (warp 8), V tiles
         // (warp 10), each as soon as its own ring has room
@@ -516,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_tmem = tmem + lane_base + L::kOCol + t * D;
         const float sl2 = a.scale_log2;
         bool ok = true;
-        int g = 0;  // score tiles of this query tile in earlier units
+        int g = 0;   // score tiles of this query tile in earlier units
+        int un = 0;  // earlier units with rows in this query tile
         const uint32_t s_tmem = tmem + lane_base + s_col(t);
         for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
             const int n = u.ps.tiles(t);
@@ -628,34 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[B_PREADY + t]);
             }
             if (!ok) break;
-            const int Gl = g + n - 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], Gl & 1));
-            if (!ok) break;
-            tc::fence_after();
-            const bool row_valid = r < u.ps.rows(t);
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.out + ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t orr[32];
-                tc::ld32(o_tmem + c * 32, orr);
-                if (row_valid) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __half2 hv = __floats2half2_rn(u2f(orr[v * 8 + 2 * e]) * inv,
-                                                                 u2f(orr[v * 8 + 2 * e + 1]) * inv);
-                            w[e] = *reinterpret_cast<const uint32_t *>(&hv);
-                        }
-                        dst[c * 4 + v] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
-            }
-            tc::fence_before();
-            mbar_arrive(&bar[B_OFREE + t]);  // O_t has been read: the next unit may overwrite it
+            // The row sum goes to the output warpgroup, which waits for the
+            // unit's last P.V; this warpgroup goes on to the next unit.
+            lsum[(2 * t + (un & 1)) * 128 + r] = l;
+            mbar_arrive(&bar[B_LREADY + 2 * t + (un & 1)]);
+            ++un;
             g += n;
         }
         if (!ok && lane == 0) report(a.status, PA_DEV_TIMEOUT);
