@@ -12,10 +12,12 @@
 // (8 cache blocks) past a tile's last row are never loaded, and only the
 // tiles that reach past a tile's first row are masked.
 //
-// Schedule: units are ordered (sequence, head, row pair) and dealt round
-// robin to the CTAs of a persistent grid, so the CTAs running at any moment
+// Schedule: units are ordered (sequence, head, row pair from the last to the
+// first) and handed out in that order by a global work counter to the CTAs
+// of a persistent grid as they become free, so the CTAs running at any moment
 // work on neighbouring units, mostly of the same heads, and read each K/V
-// tile from L2 rather than each from HBM.
+// tile from L2 rather than each from HBM; the costliest pair of a head goes
+// first and the cheap ones close the list, which evens out the CTAs' ends.
 //
 // Roles (512 threads):
 //   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
@@ -26,7 +28,8 @@
 //               2 stages, V: 3 when shared memory allows, else 2), each
 //               refilled as soon as its own slot is free
 //   warp 9      MMA issuer (one thread) and TMEM owner
-//   warp 11     idle
+//   warp 11     scheduler: takes the CTA's next units from the launch's
+//               work counter into a ring in shared memory
 //   warps 12-15 output: O_t / l of a finished tile to global memory, while
 //               the softmax warpgroups already work on the next unit
 // Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
@@ -46,6 +49,8 @@
 //
 // Bound: tensor cores.  Algorithmic FLOPs = 4 * d * H * (number of visible
 // (query, key) pairs).
+#include <atomic>
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -68,6 +73,17 @@ constexpr int kThreads = 16 * 32;  // 128 registers per thread, no spills
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSeqs = 2048;
+constexpr int kSchedWarp = 11;
+constexpr int kRing = 8;             // scheduled units buffered per CTA
+constexpr int kRingConsumers = 15;   // warps that read every ring entry
+constexpr int kRingByte = 384;       // offset of the ring in the barrier area
+constexpr int kSchedSlots = 64;      // launches that may run at the same time
+
+// Work counters of the dynamic unit schedule, one pair per launch slot: the
+// next unit to hand out, and the CTAs that took their last unit (the last of
+// them resets both for the slot's next launch).
+__device__ int g_sched_next[kSchedSlots];
+__device__ int g_sched_done[kSchedSlots];
 
 struct PrefillArgs {
     const int32_t *cu_q;
@@ -77,6 +93,7 @@ struct PrefillArgs {
     int32_t *status;
     float scale_log2;
     int B, H, g, maxb, num_blocks, plane_k, plane_v, max_seqlen_q, total_q;
+    int sched;  // launch slot of the work counters
 };
 
 template <int D, int VS>
@@ -112,8 +129,12 @@ enum {
     B_OFREE = 23,   // per query tile
     B_DRAIN = 25,
     B_LREADY = 26,  // per query tile and unit parity: row sums written
-    B_COUNT = 30
+    B_UFULL = 30,   // kRing: unit ring entry written
+    B_UEMPTY = 38,  // kRing: entry read by every consumer warp
+    B_KSTART = 46,  // the K producer started a unit
+    B_COUNT = 47
 };
+static_assert(B_COUNT * 8 + 4 <= kRingByte && kRingByte + kRing * 4 <= 512, "barrier area");
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2, int c3) {
@@ -164,12 +185,13 @@ __device__ __forceinline__ bool seq_ok(const PrefillArgs &a, const SeqInfo &si) 
            si.q_begin >= 0 && si.q_begin + si.L_q <= a.total_q;
 }
 
-// The units (s, h, k) of one CTA: unit indices blockIdx.x, blockIdx.x + G,
-// ... of the list ordered (sequence, head, row pair), so the CTAs running at
-// any moment work on neighbouring units, mostly of the same heads, and share
-// those heads' K/V tiles in L2.  `tab` is the shared-memory sequence table:
-// tab[s] = {units of sequences before s, q_begin, L_q, k_len}, tab[B].x =
-// all units.
+// Work unit idx of the list ordered (sequence, head, row pair from the last
+// to the first).  CTAs take units from the list in order as they finish
+// others, so the CTAs running at any moment work on neighbouring units,
+// mostly of the same heads, and share those heads' K/V tiles in L2; within a
+// head the costliest pair comes first, so the list ends on cheap units.
+// `tab` is the shared-memory sequence table: tab[s] = {units of sequences
+// before s, q_begin, L_q, k_len}, tab[B].x = all units.
 struct UnitIter {
     int u;  // unit index
     int s, h, k;
@@ -197,12 +219,21 @@ struct UnitIter {
         npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
         const int rem = u - e.x;
         h = rem / npairs;
-        k = rem - h * npairs;
+        k = npairs - 1 - (rem - h * npairs);
         ps = pair_shape(p, si.L_q, k);
     }
-    __device__ __forceinline__ void next(int B, const int4 *tab) { set(B, tab, u + gridDim.x); }
     __device__ __forceinline__ bool valid(int B, const int4 *tab) const { return u < tab[B].x; }
 };
+
+// A CTA that has taken its last unit; the last such CTA of the launch clears
+// the slot's counters for the next launch that uses it.
+__device__ __forceinline__ void sched_finish(int slot) {
+    __threadfence();
+    if (atomicAdd(&g_sched_done[slot], 1) == (int)gridDim.x - 1) {
+        atomicExch(&g_sched_next[slot], 0);
+        atomicExch(&g_sched_done[slot], 0);
+    }
+}
 
 template <int D, int VS>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -251,9 +282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    UnitIter first;
-    first.set(B, tab, blockIdx.x);
-    if (!first.valid(B, tab)) return;  // no unit for this CTA (whole CTA)
+    // ---- unit ring: entry 0 taken here, the rest by the scheduler warp
+    int *uring = reinterpret_cast<int *>(smem + L::kBar + kRingByte);
+    const int total_units = tab[B].x;
+    if (tid == 0) uring[0] = min(atomicAdd(&g_sched_next[a.sched], 1), total_units);
+    __syncthreads();
+    if (uring[0] >= total_units) {  // no unit left for this CTA
+        if (tid == 0) sched_finish(a.sched);
+        return;
+    }
 
     if (tid == 0) {
         for (int i = 0; i < kKStages; ++i) {
@@ -276,7 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_LREADY + 2 * i + 1], 128);
         }
         mbar_init(&bar[B_DRAIN], 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bar[B_UFULL + i], 1);
+            mbar_init(&bar[B_UEMPTY + i], kRingConsumers);
+        }
+        mbar_init(&bar[B_KSTART], 1);
         fence_barrier_init();
+        mbar_arrive(&bar[B_UFULL]);  // entry 0 is in place
     }
     if (warp == kMmaWarp) {
         tc::alloc(tmem_slot, kTmemCols);
@@ -289,6 +332,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
     float *lsum = reinterpret_cast<float *>(smem + L::kLsum);
+    // Unit of ring entry i, for lane 0 of a consumer warp: waits for the entry
+    // and releases it (one arrival per warp).
+    auto take0 = [&](int i) -> int {
+        const int slot = i % kRing;
+        if (!mbar_wait(&bar[B_UFULL + slot], (i / kRing) & 1)) {
+            report(a.status, PA_DEV_TIMEOUT);
+            return INT_MAX;
+        }
+        const int u = uring[slot];
+        mbar_arrive(&bar[B_UEMPTY + slot]);
+        return u;
+    };
+    auto take = [&](int i) -> int {  // the same for a whole warp
+        int u = 0;
+        if (lane == 0) u = take0(i);
+        return __shfl_sync(0xffffffffu, u, 0);
+    };
+    auto unit_at = [&](int idx) {
+        UnitIter u;
+        u.set(B, tab, idx);
+        return u;
+    };
 
     if (warp >= kEpilogueWarp) {
         // ======================= output warpgroup: thread = query row of the
@@ -300,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g0 = 0, g1 = 0;    // score tiles of query tile 0 / 1 in earlier units
         int un0 = 0, un1 = 0;  // earlier units with rows in query tile 0 / 1
-        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
+        int ui = 0;            // ring entry
+        for (UnitIter u = unit_at(take(0)); u.valid(B, tab) && ok; u = unit_at(take(++ui))) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int n = u.ps.tiles(t);
@@ -367,10 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             return blk * kBlockSize;
         };
         int kvc = 0, qn0 = 0, qn1 = 0;  // K/V tiles, Q tiles per query tile, loaded so far
-        int rows_cur = block_row(first, 0);
-        for (UnitIter u = first; u.valid(B, tab) && ok;) {
-            UnitIter un = u;  // the next unit: its first block rows are looked up early
-            un.next(B, tab);
+        int ui = 0;                     // ring entry
+        UnitIter u = unit_at(take(0)), un;
+        int rows_cur = u.valid(B, tab) ? block_row(u, 0) : 0;
+        while (u.valid(B, tab) && ok) {
+            // Starting u lets the scheduler take the unit after it: one unit
+            // ahead is enough to hide the counter's latency, and no more is
+            // claimed, so the CTAs' last units end close together.
+            if (!is_v && lane == 0) mbar_arrive(&bar[B_KSTART]);
             const int nmax = max(u.ps.n[0], u.ps.n[1]);
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
@@ -378,8 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool fix_tail = is_v && (u.si.k_len % kBlockSize) != 0 &&
                                   (nblk_k - 1) / kBlocksPerTile == nmax - 1;
             for (int j = 0; j < nmax && ok; ++j) {
-                const int rows_next = j + 1 < nmax ? block_row(u, j + 1)
-                                      : un.valid(B, tab) ? block_row(un, 0) : 0;
+                int rows_next;
+                if (j + 1 < nmax) {
+                    rows_next = block_row(u, j + 1);
+                } else {  // the next unit: its first block rows are looked up early
+                    un = unit_at(take(++ui));
+                    rows_next = un.valid(B, tab) ? block_row(un, 0) : 0;
+                }
                 const int idx = kvc + j;
                 const int st = idx % nst;
                 const uint32_t ph = (idx / nst) & 1;
@@ -501,7 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(&bar[B_KEMPTY + st]);
                 return true;
             };
-            for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
+            int ui = 0;  // ring entry
+            for (UnitIter u = unit_at(take0(0)); u.valid(B, tab) && ok; u = unit_at(take0(++ui))) {
                 const int nmax = max(u.ps.n[0], u.ps.n[1]);
                 const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                 const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
@@ -565,6 +641,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bar[B_DRAIN], 0);
         }
         __syncwarp();
+      } else if (warp == kSchedWarp) {
+        // ======================= scheduler (one thread): takes the CTA's next
+        // unit from the launch's work counter into the ring once the K
+        // producer started the one before, ending with one past the last unit
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 1;; ++i) {
+                const int slot = i % kRing;
+                ok = mbar_wait(&bar[B_KSTART], (i - 1) & 1);
+                if (ok && i >= kRing) ok = mbar_wait(&bar[B_UEMPTY + slot], ((i / kRing) - 1) & 1);
+                const int u = ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units)
+                                 : total_units;
+                uring[slot] = u;
+                mbar_arrive(&bar[B_UFULL + slot]);
+                if (u >= total_units) break;
+            }
+            if (!ok) report(a.status, PA_DEV_TIMEOUT);
+            sched_finish(a.sched);
+        }
+        __syncwarp();
       }
     } else {
         // ======================= softmax warpgroups: thread = query row
@@ -577,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0;   // score tiles of this query tile in earlier units
         int un = 0;  // earlier units with rows in this query tile
         const uint32_t s_tmem = tmem + lane_base + s_col(t);
-        for (UnitIter u = first; u.valid(B, tab) && ok; u.next(B, tab)) {
+        int ui = 0;  // ring entry
+        for (UnitIter u = unit_at(take(0)); u.valid(B, tab) && ok; u = unit_at(take(++ui))) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
             const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
@@ -805,6 +902,8 @@ extern "C" int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *c
     a.plane_v = cache->layers + layer;
     a.max_seqlen_q = max_seqlen_q;
     a.total_q = total_q;
+    static std::atomic<unsigned> launches{0};
+    a.sched = (int)(launches.fetch_add(1) % kSchedSlots);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch_prefill<128>(qmap, kvmap, a, st)
                            : launch_prefill<64>(qmap, kvmap, a, st);
