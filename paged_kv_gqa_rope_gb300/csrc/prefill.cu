@@ -76,7 +76,7 @@ constexpr int kMaxSeqs = 2048;
 constexpr int kSchedWarp = 11;
 constexpr int kRing = 8;             // scheduled units buffered per CTA
 constexpr int kRingConsumers = 15;   // warps that read every ring entry
-constexpr int kRingByte = 384;       // offset of the ring in the barrier area
+constexpr int kRingByte = 512;       // offset of the ring (kRing x 32 bytes) in the barrier area
 constexpr int kSchedSlots = 64;      // launches that may run at the same time
 
 // Work counters of the dynamic unit schedule, one pair per launch slot: the
@@ -106,7 +106,7 @@ struct PL {
     static constexpr int kK = 2 * kQTile;             // kKStages stages
     static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
     static constexpr int kBar = kV + VS * kKVTile;
-    static constexpr int kLsum = kBar + 512;          // float [2 tiles][2 units][128]: row sums
+    static constexpr int kLsum = kBar + 1024;         // float [2 tiles][2 units][128]: row sums
     static constexpr int kTab = kLsum + 2048;         // int4 [B + 1]: sequence table
     static size_t bytes(int B) { return (size_t)kTab + (size_t)(B + 1) * 16; }
     static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
@@ -134,7 +134,7 @@ enum {
     B_KSTART = 46,  // the K producer started a unit
     B_COUNT = 47
 };
-static_assert(B_COUNT * 8 + 4 <= kRingByte && kRingByte + kRing * 4 <= 512, "barrier area");
+static_assert(B_COUNT * 8 + 4 <= kRingByte && kRingByte + kRing * 32 <= 1024, "barrier area");
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2, int c3) {
@@ -148,6 +148,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// Scores of columns c0 .. c0 + 63 (sa: c0 .., sb: c0 + 32 ..) past the last
+// visible column kl become -inf (diagonal tiles only).
+__device__ __forceinline__ void mask_cols(uint32_t (&sa)[32], uint32_t (&sb)[32], int c0, int kl) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (c0 + i > kl) sa[i] = f2u(-INFINITY);
+        if (c0 + 32 + i > kl) sb[i] = f2u(-INFINITY);
+    }
+}
 
 // Shape of row pair k of a sequence with L_q query rows and a prefix of p.
 struct PairShape {
@@ -196,10 +206,11 @@ struct UnitIter {
     int u;  // unit index
     int s, h, k;
     SeqInfo si;
-    int p, npairs;
+    int p;
     PairShape ps;
 
-    __device__ __forceinline__ void set(int B, const int4 *tab, int idx) {
+    // Unit idx from the sequence table (the scheduler decodes each unit once).
+    __device__ __forceinline__ void decode(int B, const int4 *tab, int idx) {
         u = idx;
         if (u >= tab[B].x) return;
         int lo = 0, hi = B - 1;  // largest s with tab[s].x <= u
@@ -215,14 +226,29 @@ struct UnitIter {
         si.q_begin = e.y;
         si.L_q = e.z;
         si.k_len = e.w;
-        p = si.k_len - si.L_q;
-        npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
+        const int npairs = (si.L_q + kUnitRows - 1) / kUnitRows;
         const int rem = u - e.x;
         h = rem / npairs;
         k = npairs - 1 - (rem - h * npairs);
+    }
+    // A decoded unit in a ring entry: {u, s, h, k}, {q_begin, L_q, k_len, 0}.
+    __device__ __forceinline__ void store(int4 *e) const {
+        e[0] = make_int4(u, s, h, k);
+        e[1] = make_int4(si.q_begin, si.L_q, si.k_len, 0);
+    }
+    __device__ __forceinline__ void load(const int4 *e) {
+        const int4 x = e[0], y = e[1];
+        u = x.x;
+        s = x.y;
+        h = x.z;
+        k = x.w;
+        si.q_begin = y.x;
+        si.L_q = y.y;
+        si.k_len = y.z;
+        p = si.k_len - si.L_q;
         ps = pair_shape(p, si.L_q, k);
     }
-    __device__ __forceinline__ bool valid(int B, const int4 *tab) const { return u < tab[B].x; }
+    __device__ __forceinline__ bool valid(int total) const { return u < total; }
 };
 
 // A CTA that has taken its last unit; the last such CTA of the launch clears
@@ -283,11 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     // ---- unit ring: entry 0 taken here, the rest by the scheduler warp
-    int *uring = reinterpret_cast<int *>(smem + L::kBar + kRingByte);
+    int4 *uring = reinterpret_cast<int4 *>(smem + L::kBar + kRingByte);  // 2 x int4 per entry
     const int total_units = tab[B].x;
-    if (tid == 0) uring[0] = min(atomicAdd(&g_sched_next[a.sched], 1), total_units);
+    if (tid == 0) {
+        UnitIter u0;
+        u0.decode(B, tab, min(atomicAdd(&g_sched_next[a.sched], 1), total_units));
+        u0.store(uring);
+    }
     __syncthreads();
-    if (uring[0] >= total_units) {  // no unit left for this CTA
+    if (uring[0].x >= total_units) {  // no unit left for this CTA
         if (tid == 0) sched_finish(a.sched);
         return;
     }
@@ -332,26 +362,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
     float *lsum = reinterpret_cast<float *>(smem + L::kLsum);
-    // Unit of ring entry i, for lane 0 of a consumer warp: waits for the entry
-    // and releases it (one arrival per warp).
-    auto take0 = [&](int i) -> int {
+    // Unit of ring entry i, for one thread of a consumer warp (the MMA
+    // issuer): waits for the entry and releases it (one arrival per warp).
+    auto take0 = [&](int i) -> UnitIter {
         const int slot = i % kRing;
+        UnitIter u;
+        u.u = INT_MAX;
         if (!mbar_wait(&bar[B_UFULL + slot], (i / kRing) & 1)) {
             report(a.status, PA_DEV_TIMEOUT);
-            return INT_MAX;
+            return u;
         }
-        const int u = uring[slot];
+        u.load(uring + 2 * slot);
         mbar_arrive(&bar[B_UEMPTY + slot]);
         return u;
     };
-    auto take = [&](int i) -> int {  // the same for a whole warp
-        int u = 0;
-        if (lane == 0) u = take0(i);
-        return __shfl_sync(0xffffffffu, u, 0);
-    };
-    auto unit_at = [&](int idx) {
+    // The same for a whole warp: every lane waits and reads, lane 0 releases.
+    auto take = [&](int i) -> UnitIter {
+        const int slot = i % kRing;
         UnitIter u;
-        u.set(B, tab, idx);
+        u.u = INT_MAX;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_UFULL + slot], (i / kRing) & 1));
+        if (ok) u.load(uring + 2 * slot);
+        __syncwarp();
+        if (lane == 0) {
+            if (ok)
+                mbar_arrive(&bar[B_UEMPTY + slot]);
+            else
+                report(a.status, PA_DEV_TIMEOUT);
+        }
         return u;
     };
 
@@ -366,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g0 = 0, g1 = 0;    // score tiles of query tile 0 / 1 in earlier units
         int un0 = 0, un1 = 0;  // earlier units with rows in query tile 0 / 1
         int ui = 0;            // ring entry
-        for (UnitIter u = unit_at(take(0)); u.valid(B, tab) && ok; u = unit_at(take(++ui))) {
+        for (UnitIter u = take(0); u.valid(total_units) && ok; u = take(++ui)) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int n = u.ps.tiles(t);
@@ -434,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int kvc = 0, qn0 = 0, qn1 = 0;  // K/V tiles, Q tiles per query tile, loaded so far
         int ui = 0;                     // ring entry
-        UnitIter u = unit_at(take(0)), un;
-        int rows_cur = u.valid(B, tab) ? block_row(u, 0) : 0;
-        while (u.valid(B, tab) && ok) {
+        UnitIter u = take(0), un;
+        int rows_cur = u.valid(total_units) ? block_row(u, 0) : 0;
+        while (u.valid(total_units) && ok) {
             // Starting u lets the scheduler take the unit after it: one unit
             // ahead is enough to hide the counter's latency, and no more is
             // claimed, so the CTAs' last units end close together.
@@ -452,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < nmax) {
                     rows_next = block_row(u, j + 1);
                 } else {  // the next unit: its first block rows are looked up early
-                    un = unit_at(take(++ui));
-                    rows_next = un.valid(B, tab) ? block_row(un, 0) : 0;
+                    un = take(++ui);
+                    rows_next = un.valid(total_units) ? block_row(un, 0) : 0;
                 }
                 const int idx = kvc + j;
                 const int st = idx % nst;
@@ -577,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             int ui = 0;  // ring entry
-            for (UnitIter u = unit_at(take0(0)); u.valid(B, tab) && ok; u = unit_at(take0(++ui))) {
+            for (UnitIter u = take0(0); u.valid(total_units) && ok; u = take0(++ui)) {
                 const int nmax = max(u.ps.n[0], u.ps.n[1]);
                 const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                 const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
@@ -651,11 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = i % kRing;
                 ok = mbar_wait(&bar[B_KSTART], (i - 1) & 1);
                 if (ok && i >= kRing) ok = mbar_wait(&bar[B_UEMPTY + slot], ((i / kRing) - 1) & 1);
-                const int u = ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units)
-                                 : total_units;
-                uring[slot] = u;
+                UnitIter u;
+                u.decode(B, tab, ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units)
+                                    : total_units);
+                u.store(uring + 2 * slot);
                 mbar_arrive(&bar[B_UFULL + slot]);
-                if (u >= total_units) break;
+                if (u.u >= total_units) break;
             }
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             sched_finish(a.sched);
@@ -674,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int un = 0;  // earlier units with rows in this query tile
         const uint32_t s_tmem = tmem + lane_base + s_col(t);
         int ui = 0;  // ring entry
-        for (UnitIter u = unit_at(take(0)); u.valid(B, tab) && ok; u = unit_at(take(++ui))) {
+        for (UnitIter u = take(0); u.valid(total_units) && ok; u = take(++ui)) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
             const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
@@ -695,21 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::ld32_issue(s_tmem + c * 32, sa);
                     tc::ld32_issue(s_tmem + c * 32 + 32, sb);
                     tc::wait_ld(sa, sb);
-                    if (!masked) {
-                        float m1 = -INFINITY;
+                    if (masked) mask_cols(sa, sb, c * 32, kl);
+                    float m1 = -INFINITY;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            mx = fmax3(mx, u2f(sa[i]), u2f(sa[i + 1]));
-                            m1 = fmax3(m1, u2f(sb[i]), u2f(sb[i + 1]));
-                        }
-                        mx = fmaxf(mx, m1);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (c * 32 + i <= kl) mx = fmaxf(mx, u2f(sa[i]));
-                            if (c * 32 + 32 + i <= kl) mx = fmaxf(mx, u2f(sb[i]));
-                        }
+                    for (int i = 0; i < 32; i += 2) {
+                        mx = fmax3(mx, u2f(sa[i]), u2f(sa[i + 1]));
+                        m1 = fmax3(m1, u2f(sb[i]), u2f(sb[i + 1]));
                     }
+                    mx = fmaxf(mx, m1);
                 }
                 const float m_tile = mx * sl2;
                 const bool raise = m_tile > m_used + kRescaleThreshold;
@@ -745,13 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::ld32_issue(s_tmem + c * 32, sa);
                     tc::ld32_issue(s_tmem + c * 32 + 32, sb);
                     tc::wait_ld(sa, sb);
-                    if (masked) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (c * 32 + i > kl) sa[i] = f2u(-INFINITY);
-                            if (c * 32 + 32 + i > kl) sb[i] = f2u(-INFINITY);
-                        }
-                    }
+                    if (masked) mask_cols(sa, sb, c * 32, kl);
                     // Pairs of columns go through one packed fp32 FMA and add.
                     uint32_t pa[16], pb[16];
 #pragma unroll
