@@ -406,7 +406,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm_flag[0] = (prev == c_last - c_first);
             }
             named_barrier_sync(1, kCons);
-            if (sm_flag[0]) {
+            const int nrec = c_last - c_first + 1;  // pieces of the pair
+            if (sm_flag[0] && nrec <= kConsumerWarps) {
+                // Merge of up to 4 pieces.  The pieces' (max, sum) per head go
+                // through shared memory (the [4][8] areas are free now), then
+                // each thread reads the O values of four of its (head, column)
+                // elements of one piece with independent loads, piece after
+                // piece, so the merge costs a few L2 round trips, not one
+                // per element.
+                __threadfence();
+                auto piece = [&](int i, int h) {
+                    const int c = c_first + i;
+                    const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                    return a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                };
+                if (tid < nrec * a.g) {
+                    const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
+                    const float *r = piece(i, h);
+                    sm_m[i * kGroupPad + h] = __ldcg(r + D);
+                    sm_l[i * kGroupPad + h] = __ldcg(r + D + 1);
+                }
+                named_barrier_sync(1, kCons);
+                // Elements tid + k * 128 (k < 8 at most), four at a time.
+                constexpr int kEl = 4;
+#pragma unroll 1
+                for (int k0 = 0; k0 < kGroupPad * D / kCons; k0 += kEl) {
+                    float Mv[kEl], Lv[kEl], Ov[kEl];
+#pragma unroll
+                    for (int k = 0; k < kEl; ++k) {
+                        const int idx = tid + (k0 + k) * kCons, h = idx / D;
+                        Mv[k] = -INFINITY;
+                        Lv[k] = Ov[k] = 0.f;
+                        if (idx < a.g * D)
+                            for (int i = 0; i < nrec; ++i)
+                                Mv[k] = fmaxf(Mv[k], sm_m[i * kGroupPad + h]);
+                    }
+                    for (int i = 0; i < nrec; ++i) {
+                        float x[kEl];
+#pragma unroll
+                        for (int k = 0; k < kEl; ++k) {
+                            const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
+                            x[k] = idx < a.g * D ? __ldcg(piece(i, h) + d) : 0.f;
+                        }
+#pragma unroll
+                        for (int k = 0; k < kEl; ++k) {
+                            const int idx = tid + (k0 + k) * kCons, h = idx / D;
+                            if (idx < a.g * D && Mv[k] != -INFINITY) {
+                                const float f = ex2(sm_m[i * kGroupPad + h] - Mv[k]);
+                                Lv[k] += f * sm_l[i * kGroupPad + h];
+                                Ov[k] += f * x[k];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < kEl; ++k) {
+                        const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
+                        if (idx < a.g * D)
+                            a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
+                                __float2half_rn(Lv[k] > 0.f ? Ov[k] / Lv[k] : 0.f);
+                    }
+                }
+                if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
+            } else if (sm_flag[0]) {
+                // More pieces (a long pair over a narrow grid): one element at
+                // a time.
                 __threadfence();
                 for (int idx = tid; idx < a.g * D; idx += kCons) {
                     const int h = idx / D, d = idx - (idx / D) * D;
