@@ -260,6 +260,53 @@ int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,
                       int head_dim, float scale, void *out, int32_t *dev_status,
                       pa_stream_t stream);
 
+/*
+ * One decode step of a batch in one call: pa_rope_kv_write of the batch's
+ * new tokens (one per sequence) followed by pa_decode, the two kernels
+ * chained so that the decode kernel's set-up overlaps the RoPE/append
+ * kernel (programmatic dependent launch; the decode kernel waits for the
+ * append's writes before it reads Q or the cache).  The serving loop of
+ * "nano-vllm notes - Llama" (prepare_decode, then the attention call with
+ * context_lens) does these two things every step; the page captures such a
+ * decode step in a CUDA graph, which pa_step_graph_create below does with
+ * this call.
+ *   q, k, v            device fp16 [num_seqs][n_heads | n_kv_heads][head_dim]
+ *                      (q and k rotated in place)
+ *   positions, slot_mapping, context_lens   device int32 [num_seqs]
+ * Every other argument, the results and the device-side checks are those of
+ * pa_rope_kv_write (num_tokens = num_seqs) and pa_decode; the first error
+ * stops the call.  Allocates nothing and never synchronises.
+ */
+int pa_decode_step(void *q, void *k, const void *v, const int32_t *positions,
+                   const int32_t *slot_mapping, const void *rope_table, int max_positions,
+                   const pa_cache_t *cache, int layer, const int32_t *block_tables,
+                   int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                   int n_heads, int n_kv_heads, int head_dim, float scale, void *workspace,
+                   size_t workspace_bytes, void *out, int32_t *dev_status, pa_stream_t stream);
+
+/*
+ * A decode step captured once into an executable CUDA graph and replayed
+ * per step: pa_step_graph_create records pa_decode_step with the given
+ * arguments (on a stream of its own, in relaxed capture mode) and
+ * instantiates it; pa_step_graph_launch replays it on `stream`.  The replay
+ * uses the same device buffers, batch size and shapes; what the buffers
+ * hold (new tokens, positions, slots, context lengths, block tables) may
+ * change between replays, as in a serving loop.  The caller keeps every
+ * buffer alive and unchanged in size until pa_step_graph_destroy.  Errors: those of pa_decode_step found at capture (nothing is
+ * created), PA_ERR_CUDA if capture or instantiation fails, PA_ERR_INVALID
+ * for a NULL handle.
+ */
+typedef struct pa_step_graph *pa_step_graph_t;
+int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, const void *v,
+                         const int32_t *positions, const int32_t *slot_mapping,
+                         const void *rope_table, int max_positions, const pa_cache_t *cache,
+                         int layer, const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                         int head_dim, float scale, void *workspace, size_t workspace_bytes,
+                         void *out, int32_t *dev_status);
+int pa_step_graph_launch(pa_step_graph_t graph, pa_stream_t stream);
+int pa_step_graph_destroy(pa_step_graph_t graph);
+
 /* Human-readable text of a pa_status code. */
 const char *pa_strerror(int code);
 

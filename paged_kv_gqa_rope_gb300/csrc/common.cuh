@@ -178,6 +178,17 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched
+// with programmatic stream serialization may start while the kernel before
+// it in the stream still runs; `griddep_wait` returns once that kernel has
+// completed and its writes are visible (at once for an ordinary launch).
+// `griddep_launch_dependents` lets such a dependent kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
+    // Everything above read only call metadata; Q and the cache may still be
+    // being written by the RoPE/append kernel before this one.
+    griddep_wait();
     const int64_t W = prefix[B];
     // With fewer blocks than CTAs only the first W CTAs get a (one-block)
     // range, so that every range is non-empty and a pair cut into pieces
@@ -543,7 +546,7 @@ int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_gr
     }
     const int grid = min(sm_count() * per_sm, max_grid);
     if (grid < 1) return PA_ERR_CUDA;
-    decode_kernel<D, NSTAGE><<<grid, kThreads, smem, st>>>(map, a);
+    launch_dependent(decode_kernel<D, NSTAGE>, dim3(grid), dim3(kThreads), smem, st, map, a);
     return launch_status();
 }
 

@@ -1,6 +1,8 @@
 // Host-side helpers shared by the translation units of libpa.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -34,6 +36,26 @@ inline int launch_status() {
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Launch `kernel` with programmatic stream serialization: it may start while
+// the previous kernel in the stream finishes, and must call griddep_wait()
+// before it reads anything that kernel writes.  An error is left for
+// launch_status().
+template <typename... Params, typename... Args>
+inline void launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // cuTensorMapEncodeTiled obtained from the driver at run time (the library
 // does not link libcuda, so it loads on machines without a GPU).

@@ -358,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // The set-up above read only call metadata; Q and the cache may still be
+    // being written by the RoPE/append kernel before this one.
+    griddep_wait();
     const uint32_t tmem = *tmem_slot;
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
@@ -871,7 +874,8 @@ int launch_prefill_vs(const CUtensorMap &qmap, const CUtensorMap &kvmap, const P
     }
     const int grid = sm_count();
     if (grid < 1) return PA_ERR_CUDA;
-    prefill_kernel<D, VS><<<grid, kThreads, prefill_smem<D, VS>(a.B), st>>>(qmap, kvmap, a);
+    launch_dependent(prefill_kernel<D, VS>, dim3(grid), dim3(kThreads), prefill_smem<D, VS>(a.B),
+                     st, qmap, kvmap, a);
     return launch_status();
 }
 

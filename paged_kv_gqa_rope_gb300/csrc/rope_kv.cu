@@ -49,6 +49,9 @@ __device__ __forceinline__ uint4 rotate8(uint4 x, const float4 cs01, const float
 
 template <int D>
 __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
+    // The decode or prefill kernel that follows may start its set-up now; it
+    // waits (griddepcontrol.wait) for this kernel's writes before using them.
+    griddep_launch_dependents();
     constexpr int kPieces = D / 8;  // 16-byte pieces per head row
     const int rows = a.n_heads + 2 * a.n_kv_heads;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

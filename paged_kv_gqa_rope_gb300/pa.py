@@ -24,7 +24,8 @@ EXPORTS = (
     "pa_cache_bytes", "pa_alloc_cache", "pa_free_cache", "pa_prepare_prefill",
     "pa_prepare_decode", "pa_rope_table_bytes", "pa_rope_table_init", "pa_rope_kv_write",
     "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
-    "pa_check_device", "pa_decode_noalloc",
+    "pa_check_device", "pa_decode_noalloc", "pa_decode_step", "pa_step_graph_create",
+    "pa_step_graph_launch", "pa_step_graph_destroy",
 )
 
 
@@ -62,6 +63,14 @@ _SIGS = {
                          _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
                                  _i32, _i32, ctypes.c_float, _vp, _vp, _vp]),
+    "pa_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(PaCache), _i32,
+                              _vp, _i32, _vp, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _sz,
+                              _vp, _vp, _vp]),
+    "pa_step_graph_create": (_i32, [ctypes.POINTER(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                    ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
+                                    _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp]),
+    "pa_step_graph_launch": (_i32, [_vp, _vp]),
+    "pa_step_graph_destroy": (_i32, [_vp]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
     "pa_check_device": (_i32, []),
 }
@@ -246,3 +255,62 @@ def decode(q, cache: Cache, block_tables, context_lens, workspace, n_kv_heads, l
         _p(context_lens), B, H, n_kv_heads, d, float(scale), _p(workspace), workspace.numel(),
         _p(out), _p(status), _stream(stream)))
     return out
+
+
+def _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables, context_lens,
+               workspace, n_kv_heads, layer, scale, out, status):
+    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
+    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
+    _dev(rope_table, torch.float32, "rope_table"); _dev(block_tables, torch.int32, "block_tables")
+    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
+    B, H, d = q.shape
+    return [_p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), _p(rope_table),
+            rope_table.shape[0], ctypes.byref(cache.desc), layer, _p(block_tables),
+            block_tables.shape[1], _p(context_lens), B, H, n_kv_heads, d, float(scale),
+            _p(workspace), workspace.numel(), _p(out), _p(status)]
+
+
+def decode_step(q, k, v, positions, slot_mapping, rope_table, cache: Cache, block_tables,
+                context_lens, workspace, n_kv_heads, layer=0, scale=0.0, out=None, status=None,
+                stream=None):
+    """pa_decode_step: RoPE + append of the new tokens, then decode."""
+    if out is None:
+        out = torch.empty_like(q)
+    args = _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
+                      context_lens, workspace, n_kv_heads, layer, scale, out, status)
+    _check("pa_decode_step", lib().pa_decode_step(*args, _stream(stream)))
+    return out
+
+
+class StepGraph:
+    """pa_step_graph_*: a decode step captured once, replayed by launch().
+    The tensors passed in are the step's buffers for every replay; refill
+    them in place between replays.  References are kept so they outlive
+    the graph."""
+
+    def __init__(self, q, k, v, positions, slot_mapping, rope_table, cache: Cache, block_tables,
+                 context_lens, workspace, n_kv_heads, layer=0, scale=0.0, out=None,
+                 status=None):
+        self.out = torch.empty_like(q) if out is None else out
+        self._keep = (q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
+                      context_lens, workspace, status)
+        args = _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
+                          context_lens, workspace, n_kv_heads, layer, scale, self.out, status)
+        h = ctypes.c_void_p()
+        _check("pa_step_graph_create", lib().pa_step_graph_create(ctypes.byref(h), *args))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check("pa_step_graph_launch", lib().pa_step_graph_launch(self._h, _stream(stream)))
+        return self.out
+
+    def close(self):
+        if self._h:
+            _check("pa_step_graph_destroy", lib().pa_step_graph_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -111,3 +111,10 @@ def test_kernel_entry_points_validate_before_launch(libpa):
     assert libpa.pa_prefill_varlen(buf, 0, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 64, 0.0, buf, None, None) == pa.PA_OK
     assert libpa.pa_prefill_varlen(ctypes.c_void_p((1 << 24) + 8), 8, ctypes.byref(d), 0, buf, buf, buf, 4, 2, 16, 4, 2, 64, 0.0, buf, None, None) == pa.PA_ERR_INVALID
     assert libpa.pa_strerror(pa.PA_ERR_WORKSPACE) == b"decode workspace too small"
+
+
+def test_step_graph_rejects_null_handles(libpa):
+    assert libpa.pa_step_graph_launch(None, None) == pa.PA_ERR_INVALID
+    assert libpa.pa_step_graph_destroy(None) == pa.PA_ERR_INVALID
+    assert libpa.pa_step_graph_create(None, *([None] * 6), 0, None, 0, None, 0, None,
+                                      1, 8, 8, 128, 0.0, None, 0, None, None) == pa.PA_ERR_INVALID

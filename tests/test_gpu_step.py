@@ -1,0 +1,102 @@
+"""GPU tests of the fused decode step (pa_decode_step: RoPE/append and
+decode chained by programmatic dependent launch) and of its CUDA-graph form
+(pa_step_graph_*), replayed over consecutive steps of a serving loop with
+the buffers refilled in place ("nano-vllm notes - Llama": prepare_decode
+each step, the decode step captured in a CUDA graph)."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import reference as orc
+from paged_kv_gqa_rope_gb300 import pa
+from tests.gpu_helpers import DecodeRun, assert_attention_close, bits, oracle_decode_step
+from tests.test_gpu_decode import custom_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(libpa):
+    assert torch.cuda.is_available()
+    assert pa.check_device() == pa.PA_OK
+    return libpa
+
+
+def fused(run):
+    wl = run.wl
+    return pa.decode_step(run.q, run.k, run.v, run.positions, run.slots, run.table, run.cache,
+                          run.bt, run.ctx, run.ws, wl.n_kv_heads, status=run.status)
+
+
+def test_decode_step_equals_separate_calls():
+    case, init = custom_case(32, 8, 128, [5, 100, 1000, 2999, 40000], seed=21)
+    sep = DecodeRun(case, init)
+    want_out = sep.run()
+    one = DecodeRun(case, init)
+    got = fused(one)
+    torch.cuda.synchronize()
+    assert int(one.status.item()) == 0
+    assert torch.equal(got, want_out)
+    assert torch.equal(one.cache.tensor, sep.cache.tensor)
+    assert torch.equal(one.q, sep.q)
+    _, _, _, want = oracle_decode_step(case, init)
+    assert_attention_close(got, want)
+
+
+def next_step(case, rng):
+    """The same sequences one token later: new q/k/v, one more cached token."""
+    wl = case.wl
+    B = len(case.num_cached)
+    q = rng.standard_normal((B, wl.n_heads, wl.head_dim), dtype=np.float32).astype(np.float16)
+    k = rng.standard_normal((B, wl.n_kv_heads, wl.head_dim), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((B, wl.n_kv_heads, wl.head_dim), dtype=np.float32).astype(np.float16)
+    return dataclasses.replace(case, num_cached=case.num_cached + 1, q=q, k=k, v=v)
+
+
+def test_step_graph_replays_a_serving_loop():
+    ctxs = [5, 100, 1000, 2999]  # (c + 3) stays inside each sequence's blocks
+    case, init = custom_case(16, 4, 128, ctxs, seed=22)
+    run = DecodeRun(case, init, table_rows=4096)
+    g = pa.StepGraph(run.q, run.k, run.v, run.positions, run.slots, run.table, run.cache,
+                     run.bt, run.ctx, run.ws, case.wl.n_kv_heads, status=run.status)
+    rng = np.random.default_rng(23)
+    cache_np = init
+    try:
+        for step in range(3):
+            out = g.launch()
+            torch.cuda.synchronize()
+            assert int(run.status.item()) == 0
+            q_rot, k_rot, cache_np, want = oracle_decode_step(case, cache_np)
+            assert np.array_equal(bits(run.q), bits(q_rot)), f"step {step}: rotated Q"
+            assert torch.equal(run.cache.tensor, torch.from_numpy(cache_np).cuda()), \
+                f"step {step}: cache"
+            assert_attention_close(out, want)
+            # refill the captured buffers in place for the next step
+            case = next_step(case, rng)
+            md = orc.decode_metadata(case.num_cached, case.block_tables, 16)
+            run.q.copy_(torch.from_numpy(case.q))
+            run.k.copy_(torch.from_numpy(case.k))
+            run.v.copy_(torch.from_numpy(case.v))
+            run.positions.copy_(torch.from_numpy(md["positions"].astype(np.int32)))
+            run.slots.copy_(torch.from_numpy(md["slot_mapping"].astype(np.int32)))
+            run.ctx.copy_(torch.from_numpy(md["context_lens"].astype(np.int32)))
+    finally:
+        g.close()
+
+
+def test_step_graph_launches_on_any_stream():
+    case, init = custom_case(8, 8, 64, [17, 300], seed=24)
+    a = DecodeRun(case, init)
+    want = a.run()
+    b = DecodeRun(case, init)
+    g = pa.StepGraph(b.q, b.k, b.v, b.positions, b.slots, b.table, b.cache, b.bt, b.ctx, b.ws,
+                     case.wl.n_kv_heads, status=b.status)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = g.launch(stream=s)
+    s.synchronize()
+    g.close()
+    assert torch.equal(out, want)
