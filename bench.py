@@ -196,6 +196,16 @@ class DecodeBench:
     def kernel_name(self):
         return "decode_kernel"
 
+    def graph_setup(self):
+        """The same step as pa_step_graph: captured once, replayed per step."""
+        pa, d, wl = self.pa, self.d, self.case.wl
+        self.graph = pa.StepGraph(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
+                                  self.cache, d["bt"], d["ctx"], self.ws, wl.n_kv_heads,
+                                  out=self.out, status=self.status)
+
+    def graph_step(self):
+        self.graph.launch()
+
 
 class PrefillBench:
     def __init__(self, name, dev):
@@ -314,6 +324,26 @@ def time_e2e(b, steps, warmup, dist_ctx):
     torch.cuda.synchronize()
     dist_ctx.barrier()
     return dist_ctx.max(start.elapsed_time(stop) / steps), h2d, d2h
+
+
+def time_graph(b, steps, warmup, dist_ctx):
+    """ms per step of the graph-captured decode step (RoPE/append + decode)."""
+    torch = b.torch
+    b.graph_setup()
+    for _ in range(warmup):
+        b.graph_step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        b.graph_step()
+    stop.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    b.graph.close()
+    return dist_ctx.max(start.elapsed_time(stop) / steps)
 
 
 class DistCtx:
@@ -497,6 +527,13 @@ def main():
         "clocks": clk.summary(),
         "device_status": r["status"],
     }
+    if hasattr(b, "graph_setup"):
+        g_ms = time_graph(b, steps, warmup, dctx)
+        line["step_graph"] = {"value": rate(b.units * dctx.world, g_ms / 1e3, b.unit),
+                              "unit": b.unit, "ms_per_step": g_ms, "steps": steps,
+                              "kernels_per_step": 2,
+                              "how": "pa_step_graph: RoPE/append + decode captured once "
+                                     "(programmatic dependent launch between them), replayed"}
     if not args.no_extra and dctx.world == 1:
         extra = {}
         del b
