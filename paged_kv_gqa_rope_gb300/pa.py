@@ -26,6 +26,9 @@ EXPORTS = (
     "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
     "pa_check_device", "pa_decode_noalloc", "pa_decode_step", "pa_step_graph_create",
     "pa_step_graph_launch", "pa_step_graph_destroy",
+    "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_blocks_needed", "pa_bm_allocate",
+    "pa_bm_next_chunk", "pa_bm_mark_computed", "pa_bm_can_append", "pa_bm_append",
+    "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_free",
 )
 
 
@@ -71,6 +74,18 @@ _SIGS = {
                                     _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp]),
     "pa_step_graph_launch": (_i32, [_vp, _vp]),
     "pa_step_graph_destroy": (_i32, [_vp]),
+    "pa_bm_create": (_vp, [_i32, _i32]),
+    "pa_bm_destroy": (None, [_vp]),
+    "pa_bm_num_free": (_i32, [_vp]),
+    "pa_bm_blocks_needed": (_i32, [_vp, _i32]),
+    "pa_bm_allocate": (_i32, [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)]),
+    "pa_bm_next_chunk": (_i32, [_vp, _i64, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]),
+    "pa_bm_mark_computed": (_i32, [_vp, _i64, _i32]),
+    "pa_bm_can_append": (_i32, [_vp, _i64]),
+    "pa_bm_append": (_i32, [_vp, _i64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "pa_bm_num_tokens": (_i32, [_vp, _i64]),
+    "pa_bm_block_table": (_i32, [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)]),
+    "pa_bm_free": (_i32, [_vp, _i64]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
     "pa_check_device": (_i32, []),
 }
@@ -307,6 +322,77 @@ class StepGraph:
     def close(self):
         if self._h:
             _check("pa_step_graph_destroy", lib().pa_step_graph_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class BlockManager:
+    """pa_bm_*: the host block manager (block ownership, prefix-cache reuse,
+    chunked-prefill progress); its tables feed prepare_prefill/decode."""
+
+    def __init__(self, num_blocks, block_size=16):
+        self._h = lib().pa_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise ValueError("bad block manager sizes")
+        self.block_size = block_size
+
+    def num_free(self):
+        return lib().pa_bm_num_free(self._h)
+
+    def blocks_needed(self, num_tokens):
+        return lib().pa_bm_blocks_needed(self._h, num_tokens)
+
+    def allocate(self, seq_id, tokens):
+        """Admit a prompt; returns the number of tokens already cached."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int()
+        _check("pa_bm_allocate", lib().pa_bm_allocate(self._h, seq_id, _p(t), t.size,
+                                                       ctypes.byref(n)))
+        return n.value
+
+    def next_chunk(self, seq_id, max_tokens):
+        c, n = ctypes.c_int(), ctypes.c_int()
+        _check("pa_bm_next_chunk", lib().pa_bm_next_chunk(self._h, seq_id, max_tokens,
+                                                           ctypes.byref(c), ctypes.byref(n)))
+        return c.value, n.value
+
+    def mark_computed(self, seq_id, num_tokens):
+        _check("pa_bm_mark_computed", lib().pa_bm_mark_computed(self._h, seq_id, num_tokens))
+
+    def can_append(self, seq_id):
+        r = lib().pa_bm_can_append(self._h, seq_id)
+        if r < 0:
+            raise PAError("pa_bm_can_append", -r)
+        return bool(r)
+
+    def append(self, seq_id, token):
+        """Append a decoded token; returns its cache slot."""
+        slot = ctypes.c_int32()
+        _check("pa_bm_append", lib().pa_bm_append(self._h, seq_id, int(token), ctypes.byref(slot)))
+        return slot.value
+
+    def num_tokens(self, seq_id):
+        return lib().pa_bm_num_tokens(self._h, seq_id)
+
+    def block_table(self, seq_id):
+        n = ctypes.c_int()
+        lib().pa_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(n))
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check("pa_bm_block_table", lib().pa_bm_block_table(self._h, seq_id, _p(out), out.size,
+                                                             ctypes.byref(n)))
+        return out[:n.value]
+
+    def free(self, seq_id):
+        _check("pa_bm_free", lib().pa_bm_free(self._h, seq_id))
+
+    def close(self):
+        if self._h:
+            lib().pa_bm_destroy(self._h)
             self._h = None
 
     def __del__(self):

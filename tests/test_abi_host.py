@@ -1,5 +1,5 @@
 """Host side of the C ABI, no GPU needed: the library loads and exports every
-symbol include/pa.h declares; the metadata builders agree bit for bit with
+symbol the headers under include/ declare; the metadata builders agree bit for bit with
 the oracle; invalid arguments are rejected before anything is enqueued."""
 
 import ctypes
@@ -13,13 +13,18 @@ from oracle import reference as orc
 from paged_kv_gqa_rope_gb300 import pa
 from paged_kv_gqa_rope_gb300 import workloads as W
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pa_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(INCLUDE, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pa_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(libpa):
