@@ -422,24 +422,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after();
                 const float l = lsum[slot * 128 + r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint32_t h[D / 2];  // O / l as fp16 pairs
+                const bool row_valid = r < u.ps.rows(t);
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    a.out + ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
+                // 32 columns at a time; O_t is released once its last columns
+                // are read.
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
                     tc::ld32(tmem + lane_base + L::kOCol + t * D + c * 32, orr);
+                    if (c == D / 32 - 1) {
+                        tc::fence_before();
+                        mbar_arrive(&bar[B_OFREE + t]);  // the next unit may overwrite O_t
+                    }
+                    uint32_t h[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        h[c * 16 + i] = pack_half2(u2f(orr[2 * i]) * inv, u2f(orr[2 * i + 1]) * inv);
-                }
-                tc::fence_before();
-                mbar_arrive(&bar[B_OFREE + t]);  // O_t read: the next unit may overwrite it
-                if (r < u.ps.rows(t)) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        a.out +
-                        ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
+                        h[i] = pack_half2(u2f(orr[2 * i]) * inv, u2f(orr[2 * i + 1]) * inv);
+                    if (row_valid) {
 #pragma unroll
-                    for (int v = 0; v < D / 8; ++v)
-                        dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                        for (int v = 0; v < 4; ++v)
+                            dst[c * 4 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                    }
                 }
                 g += n;
                 ++un;
