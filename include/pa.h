@@ -307,6 +307,17 @@ int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, const void *v
 int pa_step_graph_launch(pa_step_graph_t graph, pa_stream_t stream);
 int pa_step_graph_destroy(pa_step_graph_t graph);
 
+/*
+ * Self-test of the kernels' failure detection; the pages have no
+ * counterpart.  Every wait inside a libpa kernel (an mbarrier phase) is
+ * bounded: after about a second it gives up, ORs PA_DEV_TIMEOUT into the
+ * status word and lets the kernel finish, so the CUDA context stays usable.
+ * This call launches one small kernel that waits, with that same bounded
+ * wait, on a phase nothing completes: it takes about a second, then sets
+ * PA_DEV_TIMEOUT in *dev_status (device int32).  Nothing faults or hangs.
+ */
+int pa_selftest_wait_timeout(int32_t *dev_status, pa_stream_t stream);
+
 /* Human-readable text of a pa_status code. */
 const char *pa_strerror(int code);
 

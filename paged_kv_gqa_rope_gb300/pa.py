@@ -28,7 +28,7 @@ EXPORTS = (
     "pa_step_graph_launch", "pa_step_graph_destroy",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_blocks_needed", "pa_bm_allocate",
     "pa_bm_next_chunk", "pa_bm_mark_computed", "pa_bm_can_append", "pa_bm_append",
-    "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_free",
+    "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_free", "pa_selftest_wait_timeout",
 )
 
 
@@ -86,6 +86,7 @@ _SIGS = {
     "pa_bm_num_tokens": (_i32, [_vp, _i64]),
     "pa_bm_block_table": (_i32, [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)]),
     "pa_bm_free": (_i32, [_vp, _i64]),
+    "pa_selftest_wait_timeout": (_i32, [_vp, _vp]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
     "pa_check_device": (_i32, []),
 }
@@ -400,3 +401,9 @@ class BlockManager:
             self.close()
         except Exception:
             pass
+
+
+def selftest_wait_timeout(status, stream=None):
+    """pa_selftest_wait_timeout: a bounded wait that runs out (about 1 s)."""
+    _dev(status, torch.int32, "status")
+    _check("pa_selftest_wait_timeout", lib().pa_selftest_wait_timeout(_p(status), _stream(stream)))
