@@ -281,3 +281,66 @@ def attention_decode(q16, cache, layer, block_tables, context_lens,
             w = np.exp(sc - sc.max())
             out[s, h] = (w @ V[:, kv, :]) / w.sum()
     return out
+
+
+# ---------------------------------------------------------------------------
+# NEXT-4: int8 KV cache ("Meta Llama source deep-dive", 8.4: a quantised KV
+# cache stored as int8 saves memory; the page gives no scheme, so this is
+# the reading the CUDA path also follows)
+# ---------------------------------------------------------------------------
+#
+# Each (token, KV head) row x of head_dim fp16 values (K after the pinned
+# RoPE, V as given) is stored as int8 codes and one float32 scale:
+#   amax  = max_i |x_i|                       (exact in float32)
+#   scale = fl32(amax / 127)                  (0 when amax is 0)
+#   q_i   = clamp(rint(fl32(x_i / scale)), -127, 127)   rint: ties to even
+# and read back as q_i * scale.  Layout: codes [2, layers, blocks,
+# block_size, n_kv_heads, head_dim] int8; scales [2, layers, blocks,
+# n_kv_heads, block_size] float32 (a block's 16 scales of one head are
+# contiguous).
+
+def kv_quantize_int8(x16):
+    """Rows of the last axis -> (codes int8, scales float32 [...])."""
+    x = np.asarray(x16, np.float16).astype(np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    r = np.rint((x / safe[..., None]).astype(np.float32))
+    codes = np.clip(r, -127, 127).astype(np.int8)
+    codes[scale == 0] = 0
+    return codes, scale
+
+
+def new_cache_i8(layers, num_blocks, block_size, n_kv_heads, head_dim):
+    codes = np.zeros((2, layers, num_blocks, block_size, n_kv_heads, head_dim), np.int8)
+    scales = np.zeros((2, layers, num_blocks, n_kv_heads, block_size), np.float32)
+    return codes, scales
+
+
+def kv_write_i8(codes, scales, layer: int, k16, v16, slot_mapping) -> None:
+    """Quantise token t's K and V rows and store them at slot
+    slot_mapping[t] (negative: no write)."""
+    bs = codes.shape[3]
+    kq, ks = kv_quantize_int8(k16)
+    vq, vs = kv_quantize_int8(v16)
+    for t, slot in enumerate(slot_mapping):
+        slot = int(slot)
+        if slot < 0:
+            continue
+        b, r = slot // bs, slot % bs
+        codes[0, layer, b, r], codes[1, layer, b, r] = kq[t], vq[t]
+        scales[0, layer, b, :, r], scales[1, layer, b, :, r] = ks[t], vs[t]
+
+
+def dequantize_cache_i8(codes, scales) -> np.ndarray:
+    """The float64 cache the int8 one stands for: q * scale."""
+    s = np.swapaxes(scales, -1, -2)[..., None].astype(np.float64)  # [..., bs, Hk, 1]
+    return codes.astype(np.float64) * s
+
+
+def attention_decode_i8(q16, codes, scales, layer, block_tables, context_lens,
+                        n_heads, n_kv_heads, scale=None, seqs=None) -> np.ndarray:
+    """Decode against the int8 cache: the decode formula on the values the
+    codes and scales stand for."""
+    return attention_decode(q16, dequantize_cache_i8(codes, scales), layer, block_tables,
+                            context_lens, n_heads, n_kv_heads, scale=scale, seqs=seqs)

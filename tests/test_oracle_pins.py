@@ -403,3 +403,69 @@ def test_scale_argument():
     # scale 0: uniform weights over the visible keys
     for i in range(6):
         assert np.allclose(a[i, 0], V[:i + 1, 0].mean(axis=0), atol=1e-14)
+
+
+# ---------------------------------------------------------------- int8 KV cache
+
+def test_int8_quantize_worked_example():
+    """absmax 1 -> scale fl32(1/127); 0.5 / scale lands on 63.5 in float32
+    and rounds to the even 64; 0.25 -> 31.75 -> 32; zeros stay zero; a zero
+    row has scale 0 and zero codes."""
+    x = np.array([[0.5, -1.0, 0.25, 0.0], [0.0, 0.0, 0.0, 0.0]], np.float16)
+    codes, scale = orc.kv_quantize_int8(x)
+    assert codes.tolist() == [[64, -127, 32, 0], [0, 0, 0, 0]]
+    assert scale[0] == np.float32(1.0) / np.float32(127.0) and scale[1] == 0.0
+
+
+def test_int8_quantize_error_bound_and_extremes():
+    rng = np.random.default_rng(40)
+    x = (rng.standard_normal((500, 128)) * rng.uniform(0.01, 30, size=(500, 1))).astype(np.float16)
+    codes, scale = orc.kv_quantize_int8(x)
+    back = codes.astype(np.float64) * scale[:, None].astype(np.float64)
+    err = np.abs(back - x.astype(np.float64))
+    # half a step, plus the float32 rounding of the quotient (|q| <= 127
+    # units of 2^-24 each) that the rounding decision is made on
+    assert np.all(err <= scale[:, None] * (0.5 + 127 * 2.0 ** -24))
+    assert np.all(np.abs(codes).max(axis=1) == 127)     # the largest entry maps to +-127
+    assert codes.min() >= -127
+
+
+def test_int8_lossless_inputs_give_the_fp16_attention():
+    """Rows whose values are k / 128 with integer |k| <= 127 and a +-127 entry
+    quantise exactly (scale = 2^-7), so decode on the int8 cache equals
+    decode on the fp16 cache holding the same values."""
+    rng = np.random.default_rng(41)
+    bs, Hk, H, d, n = 16, 2, 4, 32, 37
+    k = rng.integers(-127, 128, size=(n, Hk, d))
+    v = rng.integers(-127, 128, size=(n, Hk, d))
+    k[..., 0], v[..., 3] = 127, -127
+    k16 = (k / 128.0).astype(np.float16)
+    v16 = (v / 128.0).astype(np.float16)
+    nb = -(-n // bs)
+    table = np.arange(nb, dtype=np.int32)[None, :]
+    slots = np.arange(n)
+    codes, scales = orc.new_cache_i8(1, nb, bs, Hk, d)
+    orc.kv_write_i8(codes, scales, 0, k16, v16, slots)
+    assert np.all(scales[:, 0, :, :, :][..., :n % bs or bs] >= 0)
+    assert np.array_equal(codes[0, 0].reshape(-1, Hk, d)[:n], k.astype(np.int8))
+    cache = orc.new_cache(1, nb, bs, Hk, d)
+    orc.kv_write(cache, 0, k16, v16, slots)
+    q = rng.standard_normal((1, H, d)).astype(np.float16)
+    a = orc.attention_decode_i8(q, codes, scales, 0, table, [n], H, Hk)
+    b = orc.attention_decode(q, cache, 0, table, [n], H, Hk)
+    assert np.allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_int8_write_places_codes_and_scales_by_slot():
+    rng = np.random.default_rng(42)
+    bs, Hk, d = 16, 3, 8
+    k16 = rng.standard_normal((3, Hk, d)).astype(np.float16)
+    v16 = rng.standard_normal((3, Hk, d)).astype(np.float16)
+    codes, scales = orc.new_cache_i8(2, 4, bs, Hk, d)
+    orc.kv_write_i8(codes, scales, 1, k16, v16, [5, -1, 3 * bs + 15])
+    kq, ks = orc.kv_quantize_int8(k16)
+    vq, vs = orc.kv_quantize_int8(v16)
+    assert np.array_equal(codes[0, 1, 0, 5], kq[0]) and np.array_equal(codes[1, 1, 3, 15], vq[2])
+    assert np.array_equal(scales[0, 1, 0, :, 5], ks[0]) and np.array_equal(scales[1, 1, 3, :, 15], vs[2])
+    assert not codes[:, 0].any() and not scales[:, 0].any()   # other layer untouched
+    assert np.count_nonzero(scales[0, 1]) == 2 * Hk            # padding token not written
