@@ -71,6 +71,14 @@ def kv_bytes(case) -> int:
     return int(ctx.sum()) * wl.n_kv_heads * wl.head_dim * 2 * 2
 
 
+def kv_bytes_i8(case) -> int:
+    """Bytes an int8-cache decode step reads: K and V codes plus one float32
+    scale per (token, KV head) for each."""
+    wl = case.wl
+    ctx = case.num_cached.astype(np.int64) + 1
+    return int(ctx.sum()) * wl.n_kv_heads * (wl.head_dim + 4) * 2
+
+
 def prefill_flops(case) -> int:
     wl = case.wl
     tot = 0
@@ -144,7 +152,7 @@ class ClockSampler:
 # ---------------------------------------------------------------- our arm
 
 class DecodeBench:
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, int8=False):
         import torch
         from paged_kv_gqa_rope_gb300 import pa
         self.pa, self.torch = pa, torch
@@ -154,8 +162,9 @@ class DecodeBench:
         md = pa.prepare_decode(case.num_cached, case.block_tables)
         self.md = md
         self.table = pa.rope_table(int(md["positions"].max()) + 1, wl.head_dim, wl.rope_theta)
-        self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
-        self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
+        if not int8:
+            self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
+            self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
         t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
         self.host = dict(q=case.q, k=case.k, v=case.v, positions=md["positions"],
                          slots=md["slot_mapping"], bt=case.block_tables, ctx=md["context_lens"])
@@ -205,6 +214,37 @@ class DecodeBench:
 
     def graph_step(self):
         self.graph.launch()
+
+
+class DecodeI8Bench(DecodeBench):
+    """The same decode step against the int8 cache (codes + scales)."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev, int8=True)
+        import torch
+        pa, case, wl = self.pa, self.case, self.case.wl
+        self.cache8 = pa.CacheI8(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
+        # Any codes and positive scales will do for timing: fill them on the GPU.
+        g = torch.Generator(device=dev).manual_seed(wl.seed)
+        self.cache8.codes.copy_(torch.randint(-127, 128, self.cache8.codes.shape, generator=g,
+                                              device=dev, dtype=torch.int8))
+        self.cache8.scales.copy_(torch.rand(self.cache8.scales.shape, generator=g, device=dev) /
+                                 64 + 1e-3)
+        self.units = kv_bytes_i8(case)
+
+    def step(self, ev=None):
+        pa, d, wl = self.pa, self.d, self.case.wl
+        pa.rope_kv_write_i8(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
+                            self.cache8, status=self.status)
+        if ev is not None:
+            ev[0].record()
+        pa.decode_i8(d["q"], self.cache8, d["bt"], d["ctx"], self.ws, wl.n_kv_heads, out=self.out,
+                     status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def kernel_name(self):
+        return "decode_kernel (int8 cache)"
 
 
 class PrefillBench:
@@ -538,11 +578,13 @@ def main():
         extra = {}
         del b
         torch.cuda.empty_cache()
-        for name in ("gqa_decode_70b", "ragged_decode", "prefill_13b"):
+        for name in ("gqa_decode_70b", "ragged_decode", "prefill_13b", "mha_decode_7b:int8",
+                     "gqa_decode_70b:int8", "ragged_decode:int8"):
             if name == args.workload:
                 continue
             try:
-                eb = make_bench(name, dev)
+                base, _, kind = name.partition(":")
+                eb = DecodeI8Bench(base, dev) if kind == "int8" else make_bench(base, dev)
                 n = 1000 if eb.unit == "GB/s" else 400
                 er = time_bench(eb, n, warmup, dctx)
                 ach = rate(eb.units, er["kernel_ms"] / 1e3, eb.unit)

@@ -318,6 +318,58 @@ int pa_step_graph_destroy(pa_step_graph_t graph);
  */
 int pa_selftest_wait_timeout(int32_t *dev_status, pa_stream_t stream);
 
+/*
+ * NEXT-4: an int8 KV cache for decode.  "Meta Llama source deep-dive", 8.4,
+ * lists a quantised (int8) KV cache among the production improvements; the
+ * page gives no scheme, so this library fixes one: every (token, KV head)
+ * row x of head_dim fp16 values (K after RoPE, V as given) is stored as
+ *     scale = fl32(max_i |x_i| / 127)       (0 for an all-zero row)
+ *     q_i   = clamp(rint(fl32(x_i / scale)), -127, 127)   (ties to even)
+ * and stands for q_i * scale.  Layout (one allocation, codes then scales):
+ *     codes  int8    [2][layers][num_blocks][block_size][n_kv_heads][head_dim]
+ *     scales float32 [2][layers][num_blocks][n_kv_heads][block_size]
+ * (a block's 16 scales of one KV head are contiguous: one 64-byte copy).
+ * A decode step reads 2 * head_dim + 8 bytes per (token, KV head) instead of
+ * 4 * head_dim.  Prefill against an int8 cache is not built.
+ */
+typedef struct {
+    int8_t *codes;        /* device pointer to codes[0][0][0][0][0][0] */
+    float *scales;        /* device pointer to scales[0][0][0][0][0] */
+    int32_t layers;
+    int32_t num_blocks;
+    int32_t block_size;   /* 16 */
+    int32_t n_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t owns;         /* 1 if pa_alloc_cache_i8 allocated it */
+} pa_cache_i8_t;
+
+/* Bytes of the pool: the codes rounded up to 256, then the scales. */
+size_t pa_cache_i8_bytes(int layers, int num_blocks, int block_size, int n_kv_heads,
+                         int head_dim);
+/* As pa_alloc_cache, for the int8 pool (device_base 256-byte aligned, at
+ * least pa_cache_i8_bytes(...) bytes, or NULL to allocate). */
+int pa_alloc_cache_i8(pa_cache_i8_t *out, int layers, int num_blocks, int block_size,
+                      int n_kv_heads, int head_dim, void *device_base);
+int pa_free_cache_i8(pa_cache_i8_t *cache);
+
+/* pa_rope_kv_write with the K/V rows quantised into the int8 pool (the
+ * codes and scale of each row as above).  Q is rotated in place exactly as
+ * by pa_rope_kv_write; arguments, results and checks are that call's. */
+int pa_rope_kv_write_i8(void *q, void *k, const void *v, const int32_t *positions,
+                        const int32_t *slot_mapping, int num_tokens, int n_heads,
+                        int n_kv_heads, int head_dim, const void *rope_table,
+                        int max_positions, const pa_cache_i8_t *cache, int layer,
+                        int32_t *dev_status, pa_stream_t stream);
+
+/* pa_decode against the int8 pool: scores use q . (codes * scale), P.V uses
+ * (codes * scale); same arguments, workspace (pa_decode_workspace_bytes),
+ * results and checks as pa_decode. */
+int pa_decode_i8(const void *q, const pa_cache_i8_t *cache, int layer,
+                 const int32_t *block_tables, int max_blocks_per_seq,
+                 const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                 int head_dim, float scale, void *workspace, size_t workspace_bytes, void *out,
+                 int32_t *dev_status, pa_stream_t stream);
+
 /* Human-readable text of a pa_status code. */
 const char *pa_strerror(int code);
 

@@ -105,6 +105,27 @@ __device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *map, int c0, 
         : "memory");
 }
 
+// ---------------------------------------------------------------- RoPE
+
+// Rotate 4 pairs with the pinned fp32 arithmetic: no contraction into FMA,
+// each product and sum rounded to fp32, the result rounded to nearest-even
+// fp16.
+__device__ __forceinline__ uint4 rope_rotate8(uint4 x, const float4 cs01, const float4 cs23) {
+    const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
+    const float s[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w[i]);
+        const float a = __low2float(h), b = __high2float(h);
+        const float re = __fsub_rn(__fmul_rn(a, c[i]), __fmul_rn(b, s[i]));
+        const float im = __fadd_rn(__fmul_rn(a, s[i]), __fmul_rn(b, c[i]));
+        __half2 r = __halves2half2(__float2half_rn(re), __float2half_rn(im));
+        w[i] = *reinterpret_cast<uint32_t *>(&r);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- warp MMA
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -187,6 +208,25 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+                 "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {

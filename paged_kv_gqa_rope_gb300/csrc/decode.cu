@@ -56,12 +56,22 @@ struct DecodeArgs {
     int32_t *status;
     float scale_log2;             // scale * log2(e)
     int B, H, Hk, g, maxb, num_blocks, plane_k, plane_v;
+    // int8 cache only: the layer's K and V scale planes [num_blocks][Hk][16]
+    const float *scales_k, *scales_v;
 };
 
-template <int D>
+// Shared memory of one ring stage.  fp16 cache: the K and V tiles of one
+// (block, KV head) as TMA writes them (128-byte swizzle).  int8 cache: the
+// K and V codes (16 rows of D bytes each), then their 16 + 16 scales.
+template <int D, bool I8 = false>
 struct Layout {
-    static constexpr int kTileBytes = kBlockSize * D * 2;  // one K or V block tile
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kTileBytes = kBlockSize * D * 2;  // one fp16 K or V block tile
+    static constexpr int kCodeBytes = kBlockSize * D;      // one int8 K or V block tile
+    static constexpr int kStageBytes =
+        I8 ? ((2 * kCodeBytes + 2 * kBlockSize * 4 + 127) / 128) * 128 : 2 * kTileBytes;
+    // int8: each consumer warp turns a stage's codes into fp16 K and V tiles
+    // of the fp16 layout here, then runs the fp16 path on them.
+    static constexpr int kWarpStaging = I8 ? 2 * kTileBytes : 0;
     static constexpr int kRec = D + 4;                     // floats per head record
 };
 
@@ -114,7 +124,42 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int piece16) {
     return (uint32_t)(line * 128 + (((piece16 & 7) ^ (line & 7)) << 4));
 }
 
-template <int D, int NSTAGE>
+// Four int8 codes -> two fp16 pairs, exactly: byte ^ 0x80 is code + 128,
+// which as the low mantissa byte of 1024.0 (0x6400) gives 1152 + code.
+__device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    w ^= 0x80808080u;
+    const uint32_t a = __byte_perm(w, 0x64u, 0x4140);  // bytes 0, 1 over 0x64
+    const uint32_t b = __byte_perm(w, 0x64u, 0x4342);  // bytes 2, 3 over 0x64
+    const __half2 off = __float2half2_rn(1152.f);
+    const __half2 x = __hsub2(*reinterpret_cast<const __half2 *>(&a), off);
+    const __half2 y = __hsub2(*reinterpret_cast<const __half2 *>(&b), off);
+    lo = *reinterpret_cast<const uint32_t *>(&x);
+    hi = *reinterpret_cast<const uint32_t *>(&y);
+}
+
+// 4-D tiled load (the int8 code map) into shared memory.
+__device__ __forceinline__ void tma_load_4d_u8(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                               int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int D, int NSTAGE, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeArgs a) {
     // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
@@ -124,12 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has not consumed yet (the mbarrier parity would alias that wait onto
     // the earlier, completed phase).
     static_assert(NSTAGE % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
-    using L = Layout<D>;
+    using L = Layout<D, I8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * L::kStageBytes);
+    uint8_t *staging = smem + NSTAGE * L::kStageBytes;  // int8: [4 warps][K, V fp16 tiles]
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + kConsumerWarps * L::kWarpStaging);
     uint64_t *empty = full + NSTAGE;
     int *stage_bad = reinterpret_cast<int *>(empty + NSTAGE);
     float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
@@ -211,11 +257,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             report(a.status, PA_DEV_TIMEOUT);
                         } else if (blk >= 0 && blk < a.num_blocks) {
                             uint8_t *dst = stages + stage * L::kStageBytes;
-                            mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-                            tma_load_5d(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
-                                        blk * kBlockSize, a.plane_k);
-                            tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0,
-                                        sg.kvh, blk * kBlockSize, a.plane_v);
+                            if constexpr (I8) {
+                                mbar_arrive_expect_tx(&full[stage],
+                                                      2 * L::kCodeBytes + 2 * kBlockSize * 4);
+                                tma_load_4d_u8(dst, &kvmap, &full[stage], 0, sg.kvh,
+                                               blk * kBlockSize, a.plane_k);
+                                tma_load_4d_u8(dst + L::kCodeBytes, &kvmap, &full[stage], 0,
+                                               sg.kvh, blk * kBlockSize, a.plane_v);
+                                const int64_t so = ((int64_t)blk * a.Hk + sg.kvh) * kBlockSize;
+                                bulk_load(dst + 2 * L::kCodeBytes, a.scales_k + so, kBlockSize * 4,
+                                          &full[stage]);
+                                bulk_load(dst + 2 * L::kCodeBytes + kBlockSize * 4, a.scales_v + so,
+                                          kBlockSize * 4, &full[stage]);
+                            } else {
+                                mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                                tma_load_5d(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
+                                            blk * kBlockSize, a.plane_k);
+                                tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0,
+                                            sg.kvh, blk * kBlockSize, a.plane_v);
+                            }
                         } else {
                             report(a.status, PA_DEV_BAD_BLOCK);
                             stage_bad[stage] = 1;
@@ -277,8 +337,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int bad = stage_bad[stage];
+            // int8: per-token scales of this lane's two score rows (tokens
+            // lane/4 and lane/4 + 8 of the block) for K and V
+            float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
+            uint32_t kt = smem_u32(stages + stage * L::kStageBytes);
+            if constexpr (I8) {
+                if (!bad) {
+                    // codes -> fp16 K and V tiles of the fp16 layout in this
+                    // warp's staging area; then the stage is free again
+                    const uint32_t src = smem_u32(stages + stage * L::kStageBytes);
+                    const uint32_t dstk = smem_u32(staging + warp * L::kWarpStaging);
+#pragma unroll 1
+                    for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll 4
+                        for (int k = 0; k < kBlockSize * (D / 8) / 32; ++k) {
+                            const int p = lane + 32 * k, row = p / (D / 8), pc = p % (D / 8);
+                            const uint2 w = ld_shared_v2(src + kv * L::kCodeBytes + row * D + pc * 8);
+                            uint32_t h0, h1, h2, h3;
+                            codes_to_half2(w.x, h0, h1);
+                            codes_to_half2(w.y, h2, h3);
+                            st_shared_v4(dstk + kv * L::kTileBytes + tile_offset<D>(row, pc), h0,
+                                         h1, h2, h3);
+                        }
+                    }
+                    const uint32_t sc = src + 2 * L::kCodeBytes + (lane >> 2) * 4;
+                    ks0 = ld_shared_f32(sc);
+                    ks1 = ld_shared_f32(sc + 32);
+                    vs0 = ld_shared_f32(sc + kBlockSize * 4);
+                    vs1 = ld_shared_f32(sc + kBlockSize * 4 + 32);
+                    kt = dstk;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (bad) stage_bad[stage] = 0;
+                    mbar_arrive(&empty[stage]);
+                }
+            }
             if (!bad) {
-                const uint32_t kt = smem_u32(stages + stage * L::kStageBytes);
                 const uint32_t vt = kt + L::kTileBytes;
                 float sc[4] = {0.f, 0.f, 0.f, 0.f};
                 const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -289,10 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_16816(sc, af, qb[kk][0], qb[kk][1]);
                 }
                 const int tok = (b0 + j) * kBlockSize + (lane >> 2);
-                float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
-                float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+                float x0 = sc[0] * (ks0 * a.scale_log2), x1 = sc[1] * (ks0 * a.scale_log2);
+                float x2 = sc[2] * (ks1 * a.scale_log2), x3 = sc[3] * (ks1 * a.scale_log2);
                 if (tok >= ctx) x0 = x1 = -INFINITY;
                 if (tok + 8 >= ctx) x2 = x3 = -INFINITY;
+                if constexpr (I8) {  // a never-written slot's scale may hold any bits
+                    if (tok >= ctx) vs0 = 0.f;
+                    if (tok + 8 >= ctx) vs1 = 0.f;
+                }
                 float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
@@ -303,10 +402,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
                 m0 = mn0;
                 m1 = mn1;
-                const __half2 p01 = __floats2half2_rn(ex2(x0 - mn0), ex2(x1 - mn1));
-                const __half2 p23 = __floats2half2_rn(ex2(x2 - mn0), ex2(x3 - mn1));
-                l0 = l0 * al0 + __low2float(p01) + __low2float(p23);
-                l1 = l1 * al1 + __high2float(p01) + __high2float(p23);
+                __half2 p01, p23;
+                if constexpr (I8) {
+                    // the row sum adds P; P.V multiplies each token's P by its
+                    // V scale (the codes stand for code * scale)
+                    const float e0 = ex2(x0 - mn0), e1 = ex2(x1 - mn1);
+                    const float e2 = ex2(x2 - mn0), e3 = ex2(x3 - mn1);
+                    l0 = l0 * al0 + e0 + e2;
+                    l1 = l1 * al1 + e1 + e3;
+                    p01 = __floats2half2_rn(e0 * vs0, e1 * vs0);
+                    p23 = __floats2half2_rn(e2 * vs1, e3 * vs1);
+                } else {
+                    p01 = __floats2half2_rn(ex2(x0 - mn0), ex2(x1 - mn1));
+                    p23 = __floats2half2_rn(ex2(x2 - mn0), ex2(x3 - mn1));
+                    l0 = l0 * al0 + __low2float(p01) + __low2float(p23);
+                    l1 = l1 * al1 + __high2float(p01) + __high2float(p23);
+                }
                 const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
                 const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
                 const int vrow = (lane & 7) + (lane >> 4) * 8;
@@ -336,10 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_16816(o[mt], af, pb0, pb1);
                 }
             }
-            __syncwarp();
-            if (lane == 0) {
-                if (bad) stage_bad[stage] = 0;
-                mbar_arrive(&empty[stage]);
+            if constexpr (!I8) {
+                __syncwarp();
+                if (lane == 0) {
+                    if (bad) stage_bad[stage] = 0;
+                    mbar_arrive(&empty[stage]);
+                }
+            } else {
+                __syncwarp();  // the staging tiles are rewritten by the next block
             }
         }
         // A timed-out wait leaves the ring out of step: every consumer warp
@@ -505,19 +620,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int NSTAGE>
+template <int D, int NSTAGE, bool I8>
 size_t decode_smem_bytes(int B) {
-    return 1024 + (size_t)NSTAGE * Layout<D>::kStageBytes + 2 * NSTAGE * sizeof(uint64_t) +
+    return 1024 + (size_t)NSTAGE * Layout<D, I8>::kStageBytes +
+           (size_t)kConsumerWarps * Layout<D, I8>::kWarpStaging + 2 * NSTAGE * sizeof(uint64_t) +
            NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
            4 * sizeof(int) + 8 + (size_t)(B + 1) * sizeof(int64_t);
 }
 
 constexpr int kStages = 8;
 
-template <int D, int NSTAGE>
+template <int D, int NSTAGE, bool I8>
 int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_grid,
                          cudaStream_t st) {
-    const size_t smem = decode_smem_bytes<D, NSTAGE>(a.B);
+    const size_t smem = decode_smem_bytes<D, NSTAGE, I8>(a.B);
     // The kernel may use up to the shared memory of kMaxSeqs sequences; the
     // limit is raised once per device.  The grid is sized from this call's
     // shared memory, so small batches get more CTAs (bytes in flight) per SM.
@@ -528,9 +644,10 @@ int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_gr
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(decode_kernel<D, NSTAGE>,
+            if (cudaFuncSetAttribute(decode_kernel<D, NSTAGE, I8>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)decode_smem_bytes<D, NSTAGE>(kMaxSeqs)) != cudaSuccess) {
+                                     (int)decode_smem_bytes<D, NSTAGE, I8>(kMaxSeqs)) !=
+                cudaSuccess) {
                 cudaGetLastError();
                 return PA_ERR_CUDA;
             }
@@ -538,15 +655,15 @@ int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_gr
         }
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NSTAGE>, kThreads,
-                                                      smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NSTAGE, I8>,
+                                                      kThreads, smem) != cudaSuccess ||
         per_sm < 1) {
         cudaGetLastError();
         return PA_ERR_CUDA;
     }
     const int grid = min(sm_count() * per_sm, max_grid);
     if (grid < 1) return PA_ERR_CUDA;
-    launch_dependent(decode_kernel<D, NSTAGE>, dim3(grid), dim3(kThreads), smem, st, map, a);
+    launch_dependent(decode_kernel<D, NSTAGE, I8>, dim3(grid), dim3(kThreads), smem, st, map, a);
     return launch_status();
 }
 
@@ -555,8 +672,11 @@ int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cud
     // 8 stages of 8 KB at d=128 and two CTAs per SM (the register budget
     // allows two) keep 128 KB of K/V in flight per SM; 4 stages, or 12-16
     // stages at one CTA per SM, measured slower on all decode workloads.
-    return launch_decode_stages<D, kStages>(map, a, max_grid, st);
+    return launch_decode_stages<D, kStages, false>(map, a, max_grid, st);
 }
+
+// int8 cache: a stage holds half the bytes, so 12 stages (two CTAs per SM).
+constexpr int kStagesI8 = 12;
 
 size_t counters_bytes(int B, int Hk) {
     return ((size_t)B * Hk * sizeof(int32_t) + 255) & ~(size_t)255;
@@ -616,9 +736,89 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     a.num_blocks = cache->num_blocks;
     a.plane_k = layer;
     a.plane_v = cache->layers + layer;
+    a.scales_k = a.scales_v = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch_decode<128>(map, a, max_grid, st)
                            : launch_decode<64>(map, a, max_grid, st);
+}
+
+// ---------------------------------------------------------------- int8 cache
+
+namespace pa {
+namespace {
+
+// 4-D uint8 map of the codes: {head_dim bytes, Hk, num_blocks * 16 rows,
+// 2 * layers planes}, box {head_dim, 1, 16, 1}, no swizzle (rows are read
+// by plain shared-memory loads and rewritten as fp16 tiles).
+bool make_codes_map(CUtensorMap *map, const pa_cache_i8_t *c) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t D = c->head_dim, Hk = c->n_kv_heads;
+    const cuuint64_t rows = (cuuint64_t)c->num_blocks * c->block_size;
+    cuuint64_t dims[4] = {D, Hk, rows, (cuuint64_t)2 * c->layers};
+    cuuint64_t strides[3] = {D, Hk * D, rows * Hk * D};
+    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kBlockSize, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, c->codes, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_i8(const void *q, const pa_cache_i8_t *cache, int layer,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs, int n_heads,
+                            int n_kv_heads, int head_dim, float scale, void *workspace,
+                            size_t workspace_bytes, void *out, int32_t *dev_status,
+                            pa_stream_t stream) {
+    if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
+        max_blocks_per_seq <= 0 || !(scale >= 0.f))
+        return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (n_heads / n_kv_heads > kGroupPad || num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+    if (!cache || !cache->codes || !cache->scales || layer < 0 || layer >= cache->layers ||
+        cache->n_kv_heads != n_kv_heads || cache->head_dim != head_dim ||
+        cache->block_size != kBlockSize || cache->num_blocks <= 0)
+        return PA_ERR_INVALID;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out || !workspace) return PA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_INVALID;
+    const size_t cnt = counters_bytes(num_seqs, n_kv_heads);
+    if (workspace_bytes < cnt + cta_record_bytes(head_dim)) return PA_ERR_WORKSPACE;
+    const size_t slots = (workspace_bytes - cnt) / cta_record_bytes(head_dim);
+    const int max_grid = (int)(slots < (size_t)kMaxGrid ? slots : (size_t)kMaxGrid);
+
+    CUtensorMap map;
+    if (!make_codes_map(&map, cache)) return PA_ERR_CUDA;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)head_dim);
+
+    DecodeArgs a;
+    a.q = static_cast<const __half *>(q);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = static_cast<__half *>(out);
+    a.counters = static_cast<int32_t *>(workspace);
+    a.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cnt);
+    a.status = dev_status;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.B = num_seqs;
+    a.H = n_heads;
+    a.Hk = n_kv_heads;
+    a.g = n_heads / n_kv_heads;
+    a.maxb = max_blocks_per_seq;
+    a.num_blocks = cache->num_blocks;
+    a.plane_k = layer;
+    a.plane_v = cache->layers + layer;
+    const int64_t plane = (int64_t)cache->num_blocks * n_kv_heads * kBlockSize;  // scales
+    a.scales_k = cache->scales + (int64_t)layer * plane;
+    a.scales_v = cache->scales + (int64_t)(cache->layers + layer) * plane;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return head_dim == 128 ? launch_decode_stages<128, kStagesI8, true>(map, a, max_grid, st)
+                           : launch_decode_stages<64, kStagesI8, true>(map, a, max_grid, st);
 }
 
 // ---------------------------------------------------------------- no-alloc variant

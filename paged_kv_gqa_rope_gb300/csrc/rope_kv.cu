@@ -28,25 +28,6 @@ struct RopeArgs {
     int num_tokens, n_heads, n_kv_heads, max_pos;
 };
 
-// Rotate 4 pairs with the pinned fp32 arithmetic: no contraction into FMA,
-// each product and sum rounded to fp32, the result rounded to nearest-even
-// fp16.
-__device__ __forceinline__ uint4 rotate8(uint4 x, const float4 cs01, const float4 cs23) {
-    const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
-    const float s[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
-    uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __half2 h = *reinterpret_cast<__half2 *>(&w[i]);
-        const float a = __low2float(h), b = __high2float(h);
-        const float re = __fsub_rn(__fmul_rn(a, c[i]), __fmul_rn(b, s[i]));
-        const float im = __fadd_rn(__fmul_rn(a, s[i]), __fmul_rn(b, c[i]));
-        __half2 r = __halves2half2(__float2half_rn(re), __float2half_rn(im));
-        w[i] = *reinterpret_cast<uint32_t *>(&r);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 template <int D>
 __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
     // The decode or prefill kernel that follows may start its set-up now; it
@@ -79,7 +60,7 @@ __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
         uint4 *p = reinterpret_cast<uint4 *>(base) + piece;
         const float4 *cs = reinterpret_cast<const float4 *>(a.table + (int64_t)pos * (D / 2) +
                                                             piece * 4);
-        const uint4 r = rotate8(*p, __ldg(cs), __ldg(cs + 1));
+        const uint4 r = rope_rotate8(*p, __ldg(cs), __ldg(cs + 1));
         *p = r;
         if (!is_q && write_cache) {
             const int h = row - a.n_heads;

@@ -29,6 +29,8 @@ EXPORTS = (
     "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_blocks_needed", "pa_bm_allocate",
     "pa_bm_next_chunk", "pa_bm_mark_computed", "pa_bm_can_append", "pa_bm_append",
     "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_free", "pa_selftest_wait_timeout",
+    "pa_cache_i8_bytes", "pa_alloc_cache_i8", "pa_free_cache_i8", "pa_rope_kv_write_i8",
+    "pa_decode_i8",
 )
 
 
@@ -38,6 +40,13 @@ class PaCache(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("owns", ctypes.c_int32), ("layer_stride", ctypes.c_int64),
                 ("kv_stride", ctypes.c_int64)]
+
+
+class PaCacheI8(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("owns", ctypes.c_int32)]
 
 
 class PAError(RuntimeError):
@@ -87,6 +96,13 @@ _SIGS = {
     "pa_bm_block_table": (_i32, [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32)]),
     "pa_bm_free": (_i32, [_vp, _i64]),
     "pa_selftest_wait_timeout": (_i32, [_vp, _vp]),
+    "pa_cache_i8_bytes": (_sz, [_i32] * 5),
+    "pa_alloc_cache_i8": (_i32, [ctypes.POINTER(PaCacheI8)] + [_i32] * 5 + [_vp]),
+    "pa_free_cache_i8": (_i32, [ctypes.POINTER(PaCacheI8)]),
+    "pa_rope_kv_write_i8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32,
+                                   ctypes.POINTER(PaCacheI8), _i32, _vp, _vp]),
+    "pa_decode_i8": (_i32, [_vp, ctypes.POINTER(PaCacheI8), _i32, _vp, _i32, _vp, _i32, _i32,
+                            _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp]),
     "pa_strerror": (ctypes.c_char_p, [_i32]),
     "pa_check_device": (_i32, []),
 }
@@ -407,3 +423,51 @@ def selftest_wait_timeout(status, stream=None):
     """pa_selftest_wait_timeout: a bounded wait that runs out (about 1 s)."""
     _dev(status, torch.int32, "status")
     _check("pa_selftest_wait_timeout", lib().pa_selftest_wait_timeout(_p(status), _stream(stream)))
+
+
+class CacheI8:
+    """The int8 pool: ``codes`` int8 [2, layers, num_blocks, block_size,
+    n_kv_heads, head_dim] and ``scales`` float32 [2, layers, num_blocks,
+    n_kv_heads, block_size], views of one torch allocation the library
+    wraps."""
+
+    def __init__(self, layers, num_blocks, n_kv_heads, head_dim, block_size=16, device="cuda"):
+        self.desc = PaCacheI8()
+        n = lib().pa_cache_i8_bytes(layers, num_blocks, block_size, n_kv_heads, head_dim)
+        if n == 0:
+            raise ValueError("bad int8 cache shape")
+        self.buffer = torch.empty(n, dtype=torch.uint8, device=device)
+        _check("pa_alloc_cache_i8", lib().pa_alloc_cache_i8(
+            ctypes.byref(self.desc), layers, num_blocks, block_size, n_kv_heads, head_dim,
+            _p(self.buffer)))
+        nc = 2 * layers * num_blocks * block_size * n_kv_heads * head_dim
+        off = self.desc.scales - self.desc.codes
+        self.codes = self.buffer[:nc].view(torch.int8).view(
+            2, layers, num_blocks, block_size, n_kv_heads, head_dim)
+        self.scales = self.buffer[off:].view(torch.float32).view(
+            2, layers, num_blocks, n_kv_heads, block_size)
+
+
+def rope_kv_write_i8(q, k, v, positions, slot_mapping, table, cache: CacheI8, layer=0,
+                     status=None, stream=None):
+    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
+    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
+    _dev(table, torch.float32, "table")
+    T, H, d = q.shape
+    _check("pa_rope_kv_write_i8", lib().pa_rope_kv_write_i8(
+        _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), T, H, k.shape[1], d, _p(table),
+        table.shape[0], ctypes.byref(cache.desc), layer, _p(status), _stream(stream)))
+
+
+def decode_i8(q, cache: CacheI8, block_tables, context_lens, workspace, n_kv_heads, layer=0,
+              scale=0.0, out=None, status=None, stream=None):
+    _dev(q, torch.float16, "q"); _dev(block_tables, torch.int32, "block_tables")
+    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
+    B, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode_i8", lib().pa_decode_i8(
+        _p(q), ctypes.byref(cache.desc), layer, _p(block_tables), block_tables.shape[1],
+        _p(context_lens), B, H, n_kv_heads, d, float(scale), _p(workspace), workspace.numel(),
+        _p(out), _p(status), _stream(stream)))
+    return out
