@@ -301,6 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================== consumer warps
+    // int8 code conversion: this lane's fixed source and destination offsets
+    uint32_t conv_src = 0, conv_d0 = 0, conv_d1 = 0;
+    if constexpr (I8) {
+        const int pc = lane % (D / 8), row0 = lane / (D / 8);
+        const int line0 = row0 * (D / 64) + pc / 8;
+        conv_src = (uint32_t)(row0 * D + pc * 8);
+        conv_d0 = (uint32_t)(line0 * 128 + (((pc & 7) ^ (line0 & 7)) << 4));
+        conv_d1 = (uint32_t)(line0 * 128 + (((pc & 7) ^ ((line0 + 4) & 7)) << 4));
+    }
     const int head = lane >> 2;  // B-operand column (Q head in group)
     const int quad = lane & 3;
     const int h0 = 2 * quad;     // accumulator columns held by this lane
@@ -345,22 +354,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!bad) {
                     // codes -> fp16 K and V tiles of the fp16 layout in this
                     // warp's staging area; then the stage is free again
-                    const uint32_t src = smem_u32(stages + stage * L::kStageBytes);
-                    const uint32_t dstk = smem_u32(staging + warp * L::kWarpStaging);
-#pragma unroll 1
+                    // Piece k (8 codes) of this lane is row row0 + k * 256 / D,
+                    // column piece pc of its tile: source offset src_l + 256 k,
+                    // destination line line0 + 4 k (swizzle alternates by k).
+                    const uint32_t stg = smem_u32(stages + stage * L::kStageBytes);
+                    const uint32_t src = stg + conv_src;
+                    const uint32_t dst = smem_u32(staging + warp * L::kWarpStaging);
+#pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll 4
-                        for (int k = 0; k < kBlockSize * (D / 8) / 32; ++k) {
-                            const int p = lane + 32 * k, row = p / (D / 8), pc = p % (D / 8);
-                            const uint2 w = ld_shared_v2(src + kv * L::kCodeBytes + row * D + pc * 8);
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint2 w = ld_shared_v2(src + kv * L::kCodeBytes + 256 * k);
                             uint32_t h0, h1, h2, h3;
                             codes_to_half2(w.x, h0, h1);
                             codes_to_half2(w.y, h2, h3);
-                            st_shared_v4(dstk + kv * L::kTileBytes + tile_offset<D>(row, pc), h0,
-                                         h1, h2, h3);
+                            st_shared_v4(dst + kv * L::kTileBytes + ((k & 1) ? conv_d1 : conv_d0) +
+                                             512 * k,
+                                         h0, h1, h2, h3);
                         }
                     }
-                    const uint32_t sc = src + 2 * L::kCodeBytes + (lane >> 2) * 4;
+                    const uint32_t dstk = dst;
+                    const uint32_t sc = stg + 2 * L::kCodeBytes + (lane >> 2) * 4;
                     ks0 = ld_shared_f32(sc);
                     ks1 = ld_shared_f32(sc + 32);
                     vs0 = ld_shared_f32(sc + kBlockSize * 4);
