@@ -55,25 +55,26 @@ struct DecodeArgs {
     float *rec;                   // [grid][2][8][D + 4]: O (unnormalised), m, l
     int32_t *status;
     float scale_log2;             // scale * log2(e)
-    int B, H, Hk, g, maxb, num_blocks, plane_k, plane_v;
-    // int8 cache only: the layer's K and V scale planes [num_blocks][Hk][16]
-    const float *scales_k, *scales_v;
+    int B, H, Hk, g, maxb, num_blocks;
 };
 
 // Shared memory of one ring stage.  fp16 cache: the K and V tiles of one
 // (block, KV head) as TMA writes them (128-byte swizzle).  int8 cache: the
-// K and V codes (16 rows of D bytes each), then their 16 + 16 scales.
+// K and V codes (16 rows of D bytes each; 128-byte swizzle at D = 128), and
+// apart from them, in a ring of their own, the 16 K and 16 V scales.
 template <int D, bool I8 = false>
 struct Layout {
     static constexpr int kTileBytes = kBlockSize * D * 2;  // one fp16 K or V block tile
     static constexpr int kCodeBytes = kBlockSize * D;      // one int8 K or V block tile
-    static constexpr int kStageBytes =
-        I8 ? ((2 * kCodeBytes + 2 * kBlockSize * 4 + 127) / 128) * 128 : 2 * kTileBytes;
-    // int8: each consumer warp turns a stage's codes into fp16 K and V tiles
-    // of the fp16 layout here, then runs the fp16 path on them.
-    static constexpr int kWarpStaging = I8 ? 2 * kTileBytes : 0;
+    static constexpr int kStageBytes = I8 ? 2 * kCodeBytes : 2 * kTileBytes;
+    static constexpr int kScaleBytes = I8 ? 2 * kBlockSize * 4 : 0;
     static constexpr int kRec = D + 4;                     // floats per head record
 };
+
+// int8 codes enter the tensor core as fp16 code + kCodeBias (byte ^ 0x80,
+// i.e. code + 128, as the low mantissa byte of 1024.0: exact); the bias is
+// taken out of the fp32 results.
+constexpr float kCodeBias = 1152.f;
 
 // First block index of CTA c's range: floor(W * c / G).
 __device__ __forceinline__ int64_t range_start(int64_t W, int c, int G) { return W * c / G; }
@@ -124,17 +125,14 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int piece16) {
     return (uint32_t)(line * 128 + (((piece16 & 7) ^ (line & 7)) << 4));
 }
 
-// Four int8 codes -> two fp16 pairs, exactly: byte ^ 0x80 is code + 128,
-// which as the low mantissa byte of 1024.0 (0x6400) gives 1152 + code.
-__device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    w ^= 0x80808080u;
-    const uint32_t a = __byte_perm(w, 0x64u, 0x4140);  // bytes 0, 1 over 0x64
-    const uint32_t b = __byte_perm(w, 0x64u, 0x4342);  // bytes 2, 3 over 0x64
-    const __half2 off = __float2half2_rn(1152.f);
-    const __half2 x = __hsub2(*reinterpret_cast<const __half2 *>(&a), off);
-    const __half2 y = __hsub2(*reinterpret_cast<const __half2 *>(&b), off);
-    lo = *reinterpret_cast<const uint32_t *>(&x);
-    hi = *reinterpret_cast<const uint32_t *>(&y);
+// Byte offset of 16-byte chunk c of row r of an int8 code tile: rows of
+// 128 bytes with 128-byte swizzle at D = 128, plain rows at D = 64.
+template <int D>
+__device__ __forceinline__ uint32_t code_offset(int r, int c) {
+    if constexpr (D == 128)
+        return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+    else
+        return (uint32_t)(r * D + c * 16);
 }
 
 // 4-D tiled load (the int8 code map) into shared memory.
@@ -148,20 +146,20 @@ __device__ __forceinline__ void tma_load_4d_u8(void *dst, const CUtensorMap *map
         : "memory");
 }
 
-// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned) into shared memory, completion counted on `bar`.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
+// 3-D tiled load (the int8 scale map) into shared memory.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
-        "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
 
 template <int D, int NSTAGE, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap kvmap,
+                  const __grid_constant__ CUtensorMap smap, const DecodeArgs a) {
     // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
     // with a barrier of all consumer warps.  With NSTAGE a multiple of the
     // warp count, every use of a stage within a segment belongs to the same
@@ -174,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = smem;
-    uint8_t *staging = smem + NSTAGE * L::kStageBytes;  // int8: [4 warps][K, V fp16 tiles]
-    uint64_t *full = reinterpret_cast<uint64_t *>(staging + kConsumerWarps * L::kWarpStaging);
+    uint8_t *scale_ring = smem + NSTAGE * L::kStageBytes;  // int8: [NSTAGE][K 16, V 16] floats
+    uint64_t *full = reinterpret_cast<uint64_t *>(scale_ring + NSTAGE * L::kScaleBytes);
     uint64_t *empty = full + NSTAGE;
     int *stage_bad = reinterpret_cast<int *>(empty + NSTAGE);
     float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
@@ -237,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ================= producer warp: TMA block tiles into the ring
-        if (lane == 0) tma_prefetch_desc(&kvmap);
+        if (lane == 0) {
+            tma_prefetch_desc(&kvmap);
+            if constexpr (I8) tma_prefetch_desc(&smap);
+        }
         int gblk = 0;
         bool abort = false;
         for (int64_t pos = start; pos < end && !abort;) {
@@ -256,25 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) {
                             report(a.status, PA_DEV_TIMEOUT);
                         } else if (blk >= 0 && blk < a.num_blocks) {
+                            // One copy brings the block's K and V tiles (the
+                            // maps' outer dimension is the layer's K and V
+                            // planes); the int8 scales come in a second.
                             uint8_t *dst = stages + stage * L::kStageBytes;
                             if constexpr (I8) {
                                 mbar_arrive_expect_tx(&full[stage],
-                                                      2 * L::kCodeBytes + 2 * kBlockSize * 4);
+                                                      L::kStageBytes + L::kScaleBytes);
                                 tma_load_4d_u8(dst, &kvmap, &full[stage], 0, sg.kvh,
-                                               blk * kBlockSize, a.plane_k);
-                                tma_load_4d_u8(dst + L::kCodeBytes, &kvmap, &full[stage], 0,
-                                               sg.kvh, blk * kBlockSize, a.plane_v);
-                                const int64_t so = ((int64_t)blk * a.Hk + sg.kvh) * kBlockSize;
-                                bulk_load(dst + 2 * L::kCodeBytes, a.scales_k + so, kBlockSize * 4,
-                                          &full[stage]);
-                                bulk_load(dst + 2 * L::kCodeBytes + kBlockSize * 4, a.scales_v + so,
-                                          kBlockSize * 4, &full[stage]);
+                                               blk * kBlockSize, 0);
+                                tma_load_3d(scale_ring + stage * L::kScaleBytes, &smap,
+                                            &full[stage], 0, blk * a.Hk + sg.kvh, 0);
                             } else {
                                 mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
                                 tma_load_5d(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
-                                            blk * kBlockSize, a.plane_k);
-                                tma_load_5d(dst + L::kTileBytes, &kvmap, &full[stage], 0, 0,
-                                            sg.kvh, blk * kBlockSize, a.plane_v);
+                                            blk * kBlockSize, 0);
                             }
                         } else {
                             report(a.status, PA_DEV_BAD_BLOCK);
@@ -301,15 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================== consumer warps
-    // int8 code conversion: this lane's fixed source and destination offsets
-    uint32_t conv_src = 0, conv_d0 = 0, conv_d1 = 0;
-    if constexpr (I8) {
-        const int pc = lane % (D / 8), row0 = lane / (D / 8);
-        const int line0 = row0 * (D / 64) + pc / 8;
-        conv_src = (uint32_t)(row0 * D + pc * 8);
-        conv_d0 = (uint32_t)(line0 * 128 + (((pc & 7) ^ (line0 & 7)) << 4));
-        conv_d1 = (uint32_t)(line0 * 128 + (((pc & 7) ^ ((line0 + 4) & 7)) << 4));
-    }
     const int head = lane >> 2;  // B-operand column (Q head in group)
     const int quad = lane & 3;
     const int h0 = 2 * quad;     // accumulator columns held by this lane
@@ -319,22 +307,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
         const int s = sg.s, kvh = sg.kvh, b0 = sg.b0, nb = sg.nb, ctx = sg.ctx;
 
-        // Q^T fragments (B operand): Q[head][16kk + 2*quad + {0,1}] and +8.
+        // Q^T fragments (B operand).  fp16 cache: Q[head][16kk + 2*quad + {0,1}]
+        // and + 8.  int8 cache: the k order of the K fragments built from the
+        // codes (i8_k_fragment), and qbias = kCodeBias * sum over d of Q for
+        // this lane's two accumulator columns (heads h0, h0 + 1).
         uint32_t qb[D / 16][2];
+        float qbias0 = 0.f, qbias1 = 0.f;
         {
             const bool hv = head < a.g;
             const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
                 a.q + ((int64_t)s * a.H + kvh * a.g + (hv ? head : 0)) * D);
+            if constexpr (I8) {
+                float part = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                qb[kk][0] = hv ? __ldg(qrow + kk * 8 + quad) : 0u;
-                qb[kk][1] = hv ? __ldg(qrow + kk * 8 + 4 + quad) : 0u;
+                for (int m = 0; m < D / 64; ++m) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = 16 * ((D / 64) * quad + m) + 4 * i;
+                        const uint2 w = hv ? __ldg(reinterpret_cast<const uint2 *>(qrow) + d / 4)
+                                           : make_uint2(0u, 0u);
+                        qb[4 * m + i][0] = __byte_perm(w.x, w.y, 0x5410);  // Q[d], Q[d + 2]
+                        qb[4 * m + i][1] = __byte_perm(w.x, w.y, 0x7632);  // Q[d + 1], Q[d + 3]
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+                        part += (f0.x + f0.y) + (f1.x + f1.y);
+                    }
+                }
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);  // lanes 4h .. 4h+3: head h
+                qbias0 = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * quad);
+                qbias1 = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * quad + 4);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    qb[kk][0] = hv ? __ldg(qrow + kk * 8 + quad) : 0u;
+                    qb[kk][1] = hv ? __ldg(qrow + kk * 8 + 4 + quad) : 0u;
+                }
             }
         }
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         float o[D / 16][4];
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        // int8: sum over the last block's tokens of P as fed to P.V, per
+        // column.  P.V on biased codes adds kCodeBias times it to O; it is
+        // taken out again when O is rescaled for the next block, so O never
+        // carries more than one block's bias.
+        float pl0 = 0.f, pl1 = 0.f;
 
         bool abort = false;
         for (int j = warp; j < nb; j += kConsumerWarps) {
@@ -346,129 +365,186 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int bad = stage_bad[stage];
-            // int8: per-token scales of this lane's two score rows (tokens
-            // lane/4 and lane/4 + 8 of the block) for K and V
-            float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
-            uint32_t kt = smem_u32(stages + stage * L::kStageBytes);
+            const uint32_t kt = smem_u32(stages + stage * L::kStageBytes);
+            const int tok = (b0 + j) * kBlockSize + head;  // token of score row `head`
             if constexpr (I8) {
+                // This lane's codes, read once (the stage is then free again):
+                // K rows head and head + 8, chunks (D/64) quad + m; V tokens
+                // 2 quad + {0, 1, 8, 9}, the D/8 columns from head * D/8.
+                uint32_t kw[2][D / 16], vw[4][D / 32];
+                float ks0 = 0.f, ks1 = 0.f, vs0 = 0.f, vs1 = 0.f;
                 if (!bad) {
-                    // codes -> fp16 K and V tiles of the fp16 layout in this
-                    // warp's staging area; then the stage is free again
-                    // Piece k (8 codes) of this lane is row row0 + k * 256 / D,
-                    // column piece pc of its tile: source offset src_l + 256 k,
-                    // destination line line0 + 4 k (swizzle alternates by k).
-                    const uint32_t stg = smem_u32(stages + stage * L::kStageBytes);
-                    const uint32_t src = stg + conv_src;
-                    const uint32_t dst = smem_u32(staging + warp * L::kWarpStaging);
 #pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
+                    for (int r = 0; r < 2; ++r) {
 #pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint2 w = ld_shared_v2(src + kv * L::kCodeBytes + 256 * k);
-                            uint32_t h0, h1, h2, h3;
-                            codes_to_half2(w.x, h0, h1);
-                            codes_to_half2(w.y, h2, h3);
-                            st_shared_v4(dst + kv * L::kTileBytes + ((k & 1) ? conv_d1 : conv_d0) +
-                                             512 * k,
-                                         h0, h1, h2, h3);
+                        for (int m = 0; m < D / 64; ++m) {
+                            const uint4 x =
+                                ld_shared_v4(kt + code_offset<D>(head + 8 * r, (D / 64) * quad + m));
+                            kw[r][4 * m] = x.x ^ 0x80808080u;
+                            kw[r][4 * m + 1] = x.y ^ 0x80808080u;
+                            kw[r][4 * m + 2] = x.z ^ 0x80808080u;
+                            kw[r][4 * m + 3] = x.w ^ 0x80808080u;
                         }
                     }
-                    const uint32_t dstk = dst;
-                    const uint32_t sc = stg + 2 * L::kCodeBytes + (lane >> 2) * 4;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int t = 2 * quad + (v & 1) + 8 * (v >> 1);
+                        if constexpr (D == 128) {
+                            const uint4 x = ld_shared_v4(kt + L::kCodeBytes + code_offset<D>(t, head));
+                            vw[v][0] = x.x ^ 0x80808080u;
+                            vw[v][1] = x.y ^ 0x80808080u;
+                            vw[v][2] = x.z ^ 0x80808080u;
+                            vw[v][3] = x.w ^ 0x80808080u;
+                        } else {
+                            const uint2 x = ld_shared_v2(kt + L::kCodeBytes + t * D + head * (D / 8));
+                            vw[v][0] = x.x ^ 0x80808080u;
+                            vw[v][1] = x.y ^ 0x80808080u;
+                        }
+                    }
+                    const uint32_t sc = smem_u32(scale_ring + stage * L::kScaleBytes) + head * 4;
                     ks0 = ld_shared_f32(sc);
                     ks1 = ld_shared_f32(sc + 32);
                     vs0 = ld_shared_f32(sc + kBlockSize * 4);
                     vs1 = ld_shared_f32(sc + kBlockSize * 4 + 32);
-                    kt = dstk;
                 }
                 __syncwarp();
                 if (lane == 0) {
                     if (bad) stage_bad[stage] = 0;
                     mbar_arrive(&empty[stage]);
                 }
-            }
-            if (!bad) {
-                const uint32_t vt = kt + L::kTileBytes;
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+                if (!bad) {
+                    // S^T on codes + kCodeBias (exact in fp16); the bias adds
+                    // kCodeBias * sum(Q) to every score of a column.
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t af[4];
-                    ldmatrix_x4(af, kt + tile_offset<D>(krow, kk * 2 + (lane >> 4)));
-                    mma_16816(sc, af, qb[kk][0], qb[kk][1]);
-                }
-                const int tok = (b0 + j) * kBlockSize + (lane >> 2);
-                float x0 = sc[0] * (ks0 * a.scale_log2), x1 = sc[1] * (ks0 * a.scale_log2);
-                float x2 = sc[2] * (ks1 * a.scale_log2), x3 = sc[3] * (ks1 * a.scale_log2);
-                if (tok >= ctx) x0 = x1 = -INFINITY;
-                if (tok + 8 >= ctx) x2 = x3 = -INFINITY;
-                if constexpr (I8) {  // a never-written slot's scale may hold any bits
-                    if (tok >= ctx) vs0 = 0.f;
-                    if (tok + 8 >= ctx) vs1 = 0.f;
-                }
-                float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t af[4] = {__byte_perm(kw[0][kk], 0x64u, 0x4240),
+                                                __byte_perm(kw[1][kk], 0x64u, 0x4240),
+                                                __byte_perm(kw[0][kk], 0x64u, 0x4341),
+                                                __byte_perm(kw[1][kk], 0x64u, 0x4341)};
+                        mma_16816(sc, af, qb[kk][0], qb[kk][1]);
+                    }
+                    float x0 = (sc[0] - qbias0) * (ks0 * a.scale_log2);
+                    float x1 = (sc[1] - qbias1) * (ks0 * a.scale_log2);
+                    float x2 = (sc[2] - qbias0) * (ks1 * a.scale_log2);
+                    float x3 = (sc[3] - qbias1) * (ks1 * a.scale_log2);
+                    // a never-written slot's codes and scales may hold any bits
+                    if (tok >= ctx) {
+                        x0 = x1 = -INFINITY;
+                        vs0 = 0.f;
+                    }
+                    if (tok + 8 >= ctx) {
+                        x2 = x3 = -INFINITY;
+                        vs1 = 0.f;
+                    }
+                    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-                }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-                m0 = mn0;
-                m1 = mn1;
-                __half2 p01, p23;
-                if constexpr (I8) {
+                    for (int off = 4; off < 32; off <<= 1) {
+                        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                    }
+                    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                    m0 = mn0;
+                    m1 = mn1;
                     // the row sum adds P; P.V multiplies each token's P by its
                     // V scale (the codes stand for code * scale)
                     const float e0 = ex2(x0 - mn0), e1 = ex2(x1 - mn1);
                     const float e2 = ex2(x2 - mn0), e3 = ex2(x3 - mn1);
                     l0 = l0 * al0 + e0 + e2;
                     l1 = l1 * al1 + e1 + e3;
-                    p01 = __floats2half2_rn(e0 * vs0, e1 * vs0);
-                    p23 = __floats2half2_rn(e2 * vs1, e3 * vs1);
-                } else {
-                    p01 = __floats2half2_rn(ex2(x0 - mn0), ex2(x1 - mn1));
-                    p23 = __floats2half2_rn(ex2(x2 - mn0), ex2(x3 - mn1));
+                    const __half2 p01 = __floats2half2_rn(e0 * vs0, e1 * vs0);
+                    const __half2 p23 = __floats2half2_rn(e2 * vs1, e3 * vs1);
+                    const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
+                    const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
+                    const float c0 = -kCodeBias * pl0 * al0, c1 = -kCodeBias * pl1 * al1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[mt][0] = fmaf(o[mt][0], al0, c0);
+                        o[mt][1] = fmaf(o[mt][1], al1, c1);
+                        o[mt][2] = fmaf(o[mt][2], al0, c0);
+                        o[mt][3] = fmaf(o[mt][3], al1, c1);
+                        // V^T rows head*D/8 + 2 mt (+1), tokens 2 quad + {0,1}
+                        // (+8): byte 2 mt % 4 (+1) of word mt / 2 of each token
+                        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                        const uint32_t t01 = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
+                        const uint32_t t89 = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
+                        const uint32_t af[4] = {__byte_perm(t01, 0x64u, 0x4140),
+                                                __byte_perm(t01, 0x64u, 0x4342),
+                                                __byte_perm(t89, 0x64u, 0x4140),
+                                                __byte_perm(t89, 0x64u, 0x4342)};
+                        mma_16816(o[mt], af, pb0, pb1);
+                    }
+                    // this block's column sums of P, on the tensor core: 1 . P^T
+                    const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+                    float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_16816(ps, ones, pb0, pb1);
+                    pl0 = ps[0];
+                    pl1 = ps[1];
+                }
+            } else {
+                if (!bad) {
+                    const uint32_t vt = kt + L::kTileBytes;
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t af[4];
+                        ldmatrix_x4(af, kt + tile_offset<D>(krow, kk * 2 + (lane >> 4)));
+                        mma_16816(sc, af, qb[kk][0], qb[kk][1]);
+                    }
+                    float x0 = sc[0] * a.scale_log2, x1 = sc[1] * a.scale_log2;
+                    float x2 = sc[2] * a.scale_log2, x3 = sc[3] * a.scale_log2;
+                    if (tok >= ctx) x0 = x1 = -INFINITY;
+                    if (tok + 8 >= ctx) x2 = x3 = -INFINITY;
+                    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                    }
+                    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                    m0 = mn0;
+                    m1 = mn1;
+                    const __half2 p01 = __floats2half2_rn(ex2(x0 - mn0), ex2(x1 - mn1));
+                    const __half2 p23 = __floats2half2_rn(ex2(x2 - mn0), ex2(x3 - mn1));
                     l0 = l0 * al0 + __low2float(p01) + __low2float(p23);
                     l1 = l1 * al1 + __high2float(p01) + __high2float(p23);
-                }
-                const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
-                const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
-                const int vrow = (lane & 7) + (lane >> 4) * 8;
-                // Rows of V past the context (the tail of a sequence's last
-                // block) are never written and may hold any bits, NaN
-                // included; P is 0 there, but 0 * NaN is not, so those
-                // tokens' lanes of the V^T fragment are cleared.
-                const int valid = ctx - (b0 + j) * kBlockSize;  // tokens in this block
-                uint32_t keep01 = 0xffffffffu, keep89 = 0xffffffffu;
-                if (valid < kBlockSize) {
-                    const int t0 = 2 * quad;
-                    keep01 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-                    keep89 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-                }
+                    const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
+                    const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
+                    const int vrow = (lane & 7) + (lane >> 4) * 8;
+                    // Rows of V past the context (the tail of a sequence's last
+                    // block) are never written and may hold any bits, NaN
+                    // included; P is 0 there, but 0 * NaN is not, so those
+                    // tokens' lanes of the V^T fragment are cleared.
+                    const int valid = ctx - (b0 + j) * kBlockSize;  // tokens in this block
+                    uint32_t keep01 = 0xffffffffu, keep89 = 0xffffffffu;
+                    if (valid < kBlockSize) {
+                        const int t0 = 2 * quad;
+                        keep01 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                        keep89 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+                    }
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                    uint32_t af[4];
-                    ldmatrix_x4_trans(af, vt + tile_offset<D>(vrow, mt * 2 + ((lane >> 3) & 1)));
-                    af[0] &= keep01;
-                    af[1] &= keep01;
-                    af[2] &= keep89;
-                    af[3] &= keep89;
-                    mma_16816(o[mt], af, pb0, pb1);
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[mt][0] *= al0;
+                        o[mt][1] *= al1;
+                        o[mt][2] *= al0;
+                        o[mt][3] *= al1;
+                        uint32_t af[4];
+                        ldmatrix_x4_trans(af, vt + tile_offset<D>(vrow, mt * 2 + ((lane >> 3) & 1)));
+                        af[0] &= keep01;
+                        af[1] &= keep01;
+                        af[2] &= keep89;
+                        af[3] &= keep89;
+                        mma_16816(o[mt], af, pb0, pb1);
+                    }
                 }
-            }
-            if constexpr (!I8) {
                 __syncwarp();
                 if (lane == 0) {
                     if (bad) stage_bad[stage] = 0;
                     mbar_arrive(&empty[stage]);
                 }
-            } else {
-                __syncwarp();  // the staging tiles are rewritten by the next block
             }
         }
         // A timed-out wait leaves the ring out of step: every consumer warp
@@ -487,14 +563,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm_l[warp * kGroupPad + h0] = l0;
             sm_l[warp * kGroupPad + h0 + 1] = l1;
         }
+        float *ow = sm_o + (warp * kGroupPad + h0) * D;
+        if constexpr (I8) {
+            // rows head * D/8 + 2 mt and + 1 of O^T; the last block's bias out
+            const float c0 = kCodeBias * pl0, c1 = kCodeBias * pl1;
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const int d = mt * 16 + (lane >> 2);
-            float *ow = sm_o + (warp * kGroupPad + h0) * D;
-            ow[d] = o[mt][0];
-            ow[D + d] = o[mt][1];
-            ow[d + 8] = o[mt][2];
-            ow[D + d + 8] = o[mt][3];
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d = head * (D / 8) + 2 * mt;
+                ow[d] = o[mt][0] - c0;
+                ow[D + d] = o[mt][1] - c1;
+                ow[d + 1] = o[mt][2] - c0;
+                ow[D + d + 1] = o[mt][3] - c1;
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d = mt * 16 + head;
+                ow[d] = o[mt][0];
+                ow[D + d] = o[mt][1];
+                ow[d + 8] = o[mt][2];
+                ow[D + d + 8] = o[mt][3];
+            }
         }
         named_barrier_sync(1, kCons);
         abort = sm_flag[1] != 0;
@@ -637,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int NSTAGE, bool I8>
 size_t decode_smem_bytes(int B) {
     return 1024 + (size_t)NSTAGE * Layout<D, I8>::kStageBytes +
-           (size_t)kConsumerWarps * Layout<D, I8>::kWarpStaging + 2 * NSTAGE * sizeof(uint64_t) +
+           (size_t)NSTAGE * Layout<D, I8>::kScaleBytes + 2 * NSTAGE * sizeof(uint64_t) +
            NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
            4 * sizeof(int) + 8 + (size_t)(B + 1) * sizeof(int64_t);
 }
@@ -645,8 +734,8 @@ size_t decode_smem_bytes(int B) {
 constexpr int kStages = 8;
 
 template <int D, int NSTAGE, bool I8>
-int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_grid,
-                         cudaStream_t st) {
+int launch_decode_stages(const CUtensorMap &map, const CUtensorMap &smap, const DecodeArgs &a,
+                         int max_grid, cudaStream_t st) {
     const size_t smem = decode_smem_bytes<D, NSTAGE, I8>(a.B);
     // The kernel may use up to the shared memory of kMaxSeqs sequences; the
     // limit is raised once per device.  The grid is sized from this call's
@@ -677,16 +766,18 @@ int launch_decode_stages(const CUtensorMap &map, const DecodeArgs &a, int max_gr
     }
     const int grid = min(sm_count() * per_sm, max_grid);
     if (grid < 1) return PA_ERR_CUDA;
-    launch_dependent(decode_kernel<D, NSTAGE, I8>, dim3(grid), dim3(kThreads), smem, st, map, a);
+    launch_dependent(decode_kernel<D, NSTAGE, I8>, dim3(grid), dim3(kThreads), smem, st, map, smap,
+                     a);
     return launch_status();
 }
 
 template <int D>
 int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cudaStream_t st) {
+    // (no scale map on the fp16 path: the kernel never reads it)
     // 8 stages of 8 KB at d=128 and two CTAs per SM (the register budget
     // allows two) keep 128 KB of K/V in flight per SM; 4 stages, or 12-16
     // stages at one CTA per SM, measured slower on all decode workloads.
-    return launch_decode_stages<D, kStages, false>(map, a, max_grid, st);
+    return launch_decode_stages<D, kStages, false>(map, map, a, max_grid, st);
 }
 
 // int8 cache: a stage holds half the bytes, so 12 stages (two CTAs per SM).
@@ -730,7 +821,7 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     const int max_grid = (int)(slots < (size_t)kMaxGrid ? slots : (size_t)kMaxGrid);
 
     CUtensorMap map;
-    if (!make_cache_map(&map, cache, head_dim / 64, kBlockSize)) return PA_ERR_CUDA;
+    if (!make_cache_pair_map(&map, cache, layer)) return PA_ERR_CUDA;
     if (scale == 0.f) scale = 1.0f / sqrtf((float)head_dim);
 
     DecodeArgs a;
@@ -748,9 +839,6 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
     a.g = n_heads / n_kv_heads;
     a.maxb = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
-    a.plane_k = layer;
-    a.plane_v = cache->layers + layer;
-    a.scales_k = a.scales_v = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch_decode<128>(map, a, max_grid, st)
                            : launch_decode<64>(map, a, max_grid, st);
@@ -761,22 +849,43 @@ extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
 namespace pa {
 namespace {
 
-// 4-D uint8 map of the codes: {head_dim bytes, Hk, num_blocks * 16 rows,
-// 2 * layers planes}, box {head_dim, 1, 16, 1}, no swizzle (rows are read
-// by plain shared-memory loads and rewritten as fp16 tiles).
-bool make_codes_map(CUtensorMap *map, const pa_cache_i8_t *c) {
+// 4-D uint8 map of layer `layer`'s codes: {head_dim bytes, Hk, num_blocks *
+// 16 rows, 2 planes (K, V)}, box {head_dim, 1, 16, 2}: one copy brings a
+// block's K and V code tiles.  128-byte swizzle at head_dim 128 (the
+// consumers' 16-byte reads of a block tile then fall in distinct banks),
+// none at 64; L2 fetches of one row's size.
+bool make_codes_map(CUtensorMap *map, const pa_cache_i8_t *c, int layer) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
     const cuuint64_t D = c->head_dim, Hk = c->n_kv_heads;
     const cuuint64_t rows = (cuuint64_t)c->num_blocks * c->block_size;
-    cuuint64_t dims[4] = {D, Hk, rows, (cuuint64_t)2 * c->layers};
-    cuuint64_t strides[3] = {D, Hk * D, rows * Hk * D};
-    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kBlockSize, 1};
+    const cuuint64_t plane = rows * Hk * D;  // bytes of one layer's K (or V) codes
+    cuuint64_t dims[4] = {D, Hk, rows, 2};
+    cuuint64_t strides[3] = {D, Hk * D, (cuuint64_t)c->layers * plane};
+    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kBlockSize, 2};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, c->codes, dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, c->codes + (size_t)layer * plane, dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               D == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D float32 map of layer `layer`'s scales: {16, num_blocks * Hk, 2 planes
+// (K, V)}, box {16, 1, 2}: one copy brings a (block, KV head)'s 16 K and 16
+// V scales.
+bool make_scales_map(CUtensorMap *map, const pa_cache_i8_t *c, int layer) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t n = (cuuint64_t)c->num_blocks * c->n_kv_heads;
+    const cuuint64_t plane = n * kBlockSize;  // floats of one layer's K (or V) scales
+    cuuint64_t dims[3] = {(cuuint64_t)kBlockSize, n, 2};
+    cuuint64_t strides[2] = {kBlockSize * 4, (cuuint64_t)c->layers * plane * 4};
+    cuuint32_t box[3] = {(cuuint32_t)kBlockSize, 1, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c->scales + (size_t)layer * plane, dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -806,8 +915,9 @@ extern "C" int pa_decode_i8(const void *q, const pa_cache_i8_t *cache, int layer
     const size_t slots = (workspace_bytes - cnt) / cta_record_bytes(head_dim);
     const int max_grid = (int)(slots < (size_t)kMaxGrid ? slots : (size_t)kMaxGrid);
 
-    CUtensorMap map;
-    if (!make_codes_map(&map, cache)) return PA_ERR_CUDA;
+    CUtensorMap map, smap;
+    if (!make_codes_map(&map, cache, layer) || !make_scales_map(&smap, cache, layer))
+        return PA_ERR_CUDA;
     if (scale == 0.f) scale = 1.0f / sqrtf((float)head_dim);
 
     DecodeArgs a;
@@ -825,14 +935,10 @@ extern "C" int pa_decode_i8(const void *q, const pa_cache_i8_t *cache, int layer
     a.g = n_heads / n_kv_heads;
     a.maxb = max_blocks_per_seq;
     a.num_blocks = cache->num_blocks;
-    a.plane_k = layer;
-    a.plane_v = cache->layers + layer;
-    const int64_t plane = (int64_t)cache->num_blocks * n_kv_heads * kBlockSize;  // scales
-    a.scales_k = cache->scales + (int64_t)layer * plane;
-    a.scales_v = cache->scales + (int64_t)(cache->layers + layer) * plane;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return head_dim == 128 ? launch_decode_stages<128, kStagesI8, true>(map, a, max_grid, st)
-                           : launch_decode_stages<64, kStagesI8, true>(map, a, max_grid, st);
+    return head_dim == 128
+               ? launch_decode_stages<128, kStagesI8, true>(map, smap, a, max_grid, st)
+               : launch_decode_stages<64, kStagesI8, true>(map, smap, a, max_grid, st);
 }
 
 // ---------------------------------------------------------------- no-alloc variant

@@ -74,5 +74,9 @@ EncodeTiledFn encode_tiled();
 // with a box of {64, box_halves, 1, box_rows, 1} and 128-byte swizzle.
 // Plane index of (kv, layer) is kv * layers + layer.  Returns false on error.
 bool make_cache_map(CUtensorMap *map, const pa_cache_t *c, int box_halves, int box_rows);
+// The same view of one layer with dim4 = its 2 planes (K, V; stride
+// kv_stride) and a box of {64, head_dim / 64, 1, block_size, 2}: a block's
+// whole K tile, then its V tile, in one copy.
+bool make_cache_pair_map(CUtensorMap *map, const pa_cache_t *c, int layer);
 
 }  // namespace pa

@@ -47,7 +47,31 @@ bool make_cache_map(CUtensorMap *map, const pa_cache_t *c, int box_halves, int b
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, c->base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     // L2 fetches of one (token, KV head) row: 2 * head_dim bytes
+                     d >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 5-D fp16 map of layer `layer`'s K and V planes: {64, D/64, Hk, rows, 2},
+// box {64, D/64, 1, 16, 2}: one copy brings a block's K tile then its V
+// tile (each as make_cache_map's box of the whole row would).
+bool make_cache_pair_map(CUtensorMap *map, const pa_cache_t *c, int layer) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const uint64_t d = c->head_dim, hk = c->n_kv_heads;
+    const uint64_t rows = (uint64_t)c->num_blocks * c->block_size;
+    cuuint64_t dims[5] = {64, d / 64, hk, rows, 2};
+    cuuint64_t strides[4] = {128, d * 2, hk * d * 2, (uint64_t)c->kv_stride * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)(d / 64), 1, (cuuint32_t)c->block_size, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+                     static_cast<__half *>(c->base) + (size_t)layer * c->layer_stride, dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     d >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
