@@ -44,7 +44,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSeqs = 4096;
 constexpr int kGroupPad = 8;   // MMA N: Q heads per KV head, padded
-constexpr int kMaxGrid = 384;  // CTAs the workspace has record slots for
+constexpr int kMaxGrid = 456;  // CTAs the workspace has record slots for (3 per SM)
 
 struct DecodeArgs {
     const __half *q;              // [B][H][D]
@@ -156,8 +156,10 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// int8: three CTAs per SM (128 registers): the per-block consumer work, not
+// the bytes in flight, bounds the int8 pipeline, so more consumer warps pay.
 template <int D, int NSTAGE, bool I8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap,
                   const __grid_constant__ CUtensorMap smap, const DecodeArgs a) {
     // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
@@ -780,7 +782,7 @@ int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cud
     return launch_decode_stages<D, kStages, false>(map, map, a, max_grid, st);
 }
 
-// int8 cache: a stage holds half the bytes, so 12 stages (two CTAs per SM).
+// int8 cache: a stage holds half the bytes; 12 stages at three CTAs per SM.
 constexpr int kStagesI8 = 12;
 
 size_t counters_bytes(int B, int Hk) {
