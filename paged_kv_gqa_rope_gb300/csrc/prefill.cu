@@ -159,6 +159,42 @@ __device__ __forceinline__ void mask_cols(uint32_t (&sa)[32], uint32_t (&sb)[32]
     }
 }
 
+// Maximum of 64 scores (sa: columns c0 .., sb: c0 + 32 ..).
+__device__ __forceinline__ float half_max(const uint32_t (&sa)[32], const uint32_t (&sb)[32]) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        m0 = fmax3(m0, u2f(sa[i]), u2f(sa[i + 1]));
+        m1 = fmax3(m1, u2f(sa[i + 2]), u2f(sa[i + 3]));
+        m2 = fmax3(m2, u2f(sb[i]), u2f(sb[i + 1]));
+        m3 = fmax3(m3, u2f(sb[i + 2]), u2f(sb[i + 3]));
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// P = 2^(s * scale_log2 - m) of 64 scores as fp16 pairs (pa: columns c0 ..,
+// pb: c0 + 32 ..); la / lb add the fp32 values (packed pairs) before their
+// rounding.  Pairs of columns go through one packed fp32 FMA and add.
+__device__ __forceinline__ void exp_half(const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+                                         uint64_t sl2x2, float m, uint32_t (&pa)[16],
+                                         uint32_t (&pb)[16], uint64_t &la, uint64_t &lb) {
+    const uint64_t negm = f2_pack(-m, -m);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a0, a1, b0, b1;
+        f2_unpack(f2_fma(f2_pack(u2f(sa[2 * i]), u2f(sa[2 * i + 1])), sl2x2, negm), a0, a1);
+        f2_unpack(f2_fma(f2_pack(u2f(sb[2 * i]), u2f(sb[2 * i + 1])), sl2x2, negm), b0, b1);
+        a0 = ex2(a0);
+        a1 = ex2(a1);
+        b0 = ex2(b0);
+        b1 = ex2(b1);
+        la = f2_add(la, f2_pack(a0, a1));
+        lb = f2_add(lb, f2_pack(b0, b1));
+        pa[i] = pack_half2(a0, a1);
+        pb[i] = pack_half2(b0, b1);
+    }
+}
+
 // Shape of row pair k of a sequence with L_q query rows and a prefix of p.
 struct PairShape {
     int rv[2];  // valid rows of query tile 0 / 1
@@ -733,32 +769,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after();
                 const bool masked = j * kBN + kBN - 1 > first_row;
                 const int kl = key_lim - j * kBN;  // last visible column of this tile
-                // pass 1: row maximum, two 32-column loads per wait
-                float mx = -INFINITY;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                float alpha = 1.f;     // factor on O (and on l) for this tile
+                bool raised = false;   // the row's running maximum moved
+                uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
+                // Each 64-column half is read from TMEM once: its maximum
+                // (from the registers), then P over S.  A second half that
+                // raises the maximum past the threshold (rare after a row's
+                // first tile) scales the first half's P, already in TMEM.
 #pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
+                for (int hf = 0; hf < 2; ++hf) {
                     uint32_t sa[32], sb[32];
-                    tc::ld32_issue(s_tmem + c * 32, sa);
-                    tc::ld32_issue(s_tmem + c * 32 + 32, sb);
+                    tc::ld32_issue(s_tmem + hf * 64, sa);
+                    tc::ld32_issue(s_tmem + hf * 64 + 32, sb);
                     tc::wait_ld(sa, sb);
-                    if (masked) mask_cols(sa, sb, c * 32, kl);
-                    float m1 = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        mx = fmax3(mx, u2f(sa[i]), u2f(sa[i + 1]));
-                        m1 = fmax3(m1, u2f(sb[i]), u2f(sb[i + 1]));
+                    if (masked) mask_cols(sa, sb, hf * 64, kl);
+                    const float m_t = half_max(sa, sb) * sl2;
+                    const bool up = m_t > m_used + kRescaleThreshold;
+                    float a = 1.f;
+                    if (up) {
+                        a = ex2(m_used - m_t);  // 0 on the first tile
+                        l *= a;
+                        m_used = m_t;
+                        alpha *= a;
+                        raised = true;
                     }
-                    mx = fmaxf(mx, m1);
+                    {
+                        uint32_t pa[16], pb[16];
+                        exp_half(sa, sb, sl2x2, m_used, pa, pb, la, lb);
+                        tc::st16(s_tmem + hf * 32, pa);
+                        tc::st16(s_tmem + hf * 32 + 16, pb);
+                    }
+                    if (hf == 0) {  // the first half's sum joins l (scaled with it)
+                        float x0, x1, y0, y1;
+                        f2_unpack(la, x0, x1);
+                        f2_unpack(lb, y0, y1);
+                        l += (x0 + x1) + (y0 + y1);
+                        la = lb = 0;
+                    } else if (__any_sync(0xffffffffu, up)) {
+                        tc::wait_st();
+                        uint32_t p0[32];
+                        tc::ld32(s_tmem, p0);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&p0[i]));
+                            p0[i] = pack_half2(f.x * a, f.y * a);
+                        }
+                        tc::st32(s_tmem, p0);
+                    }
                 }
-                const float m_tile = mx * sl2;
-                const bool raise = m_tile > m_used + kRescaleThreshold;
-                float alpha = 1.f;
-                if (raise) {
-                    alpha = ex2(m_used - m_tile);  // 0 on the first tile
-                    l *= alpha;
-                    m_used = m_tile;
-                }
-                if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                if (j > 0 && __any_sync(0xffffffffu, raised)) {
                     // O_t must hold the previous tile's P.V before it is scaled
                     // (normally complete: S_t was issued behind it).
                     ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], (G - 1) & 1));
@@ -772,39 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * alpha);
                         tc::st32(o_tmem + c * 32, orr);
                     }
-                }
-                // pass 2: P = 2^(s*scale*log2e - m) as fp16, written over S; the
-                // row sum adds the fp32 values before rounding.
-                const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                const uint64_t negm = f2_pack(-m_used, -m_used);
-                uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    uint32_t sa[32], sb[32];
-                    tc::ld32_issue(s_tmem + c * 32, sa);
-                    tc::ld32_issue(s_tmem + c * 32 + 32, sb);
-                    tc::wait_ld(sa, sb);
-                    if (masked) mask_cols(sa, sb, c * 32, kl);
-                    // Pairs of columns go through one packed fp32 FMA and add.
-                    uint32_t pa[16], pb[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float a0, a1, b0, b1;
-                        f2_unpack(f2_fma(f2_pack(u2f(sa[2 * i]), u2f(sa[2 * i + 1])), sl2x2, negm),
-                                  a0, a1);
-                        f2_unpack(f2_fma(f2_pack(u2f(sb[2 * i]), u2f(sb[2 * i + 1])), sl2x2, negm),
-                                  b0, b1);
-                        a0 = ex2(a0);
-                        a1 = ex2(a1);
-                        b0 = ex2(b0);
-                        b1 = ex2(b1);
-                        la = f2_add(la, f2_pack(a0, a1));
-                        lb = f2_add(lb, f2_pack(b0, b1));
-                        pa[i] = pack_half2(a0, a1);
-                        pb[i] = pack_half2(b0, b1);
-                    }
-                    tc::st16(s_tmem + c * 16, pa);
-                    tc::st16(s_tmem + c * 16 + 16, pb);
                 }
                 {
                     float x0, x1, y0, y1;

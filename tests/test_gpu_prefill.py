@@ -184,3 +184,24 @@ def test_prefill_many_sequences():
     new = rng.integers(1, 40, size=B).tolist()
     case, init = custom_prefill_case(4, 2, 128, cached, new, seed=42)
     check(case, init)
+
+
+def test_prefill_rising_maximum_rescales():
+    """Keys whose norm grows with their position make later key tiles, and the
+    second half of a tile, raise a row's running maximum past the rescale
+    threshold, so the paths that rescale P (already written for a tile's
+    first half) and O run on most tiles instead of almost never."""
+    H, Hk, d = 8, 2, 128
+    cached, new = [0, 48], [700, 300]
+    case, init = custom_prefill_case(H, Hk, d, cached, new, seed=91)
+    grow = lambda p: 1.0 + np.asarray(p, np.float32) / 16.0  # noqa: E731
+    at = 0
+    for s, (c, n) in enumerate(zip(cached, new)):
+        pos = c + np.arange(n)
+        case.k[at:at + n] = (case.k[at:at + n].astype(np.float32)
+                             * grow(pos)[:, None, None]).astype(np.float16)
+        at += n
+        for p in range(c):  # the cached prefix, through the block table
+            blk, row = case.block_tables[s][p // 16], p % 16
+            init[0, 0, blk, row] = (init[0, 0, blk, row].astype(np.float32) * grow(p)).astype(np.float16)
+    check(case, init)
