@@ -246,6 +246,8 @@ class DecodeI8Bench(DecodeBench):
     def kernel_name(self):
         return "decode_kernel (int8 cache)"
 
+    graph_setup = None  # the captured step is the fp16 cache's
+
 
 class PrefillBench:
     def __init__(self, name, dev):
@@ -504,6 +506,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--int8", action="store_true",
+                    help="decode workloads: time the int8 KV cache path instead (our arm)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     dctx = DistCtx()
@@ -535,7 +539,9 @@ def main():
     from paged_kv_gqa_rope_gb300 import pa
     pa.lib()
     wl = W.WORKLOADS[args.workload]
-    b = make_bench(args.workload, dev)
+    if args.int8 and wl.kind != "decode":
+        raise SystemExit("--int8 applies to decode workloads")
+    b = DecodeI8Bench(args.workload, dev) if args.int8 else make_bench(args.workload, dev)
     steps = args.steps or (4000 if wl.kind != "prefill" else 2000)
     with ClockSampler(dctx.local) as clk:
         r = time_bench(b, steps, warmup, dctx)
@@ -554,6 +560,7 @@ def main():
         "config": {"workload": args.workload, "n_heads": wl.n_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "batch": len(b.case.num_new),
+                   "kv_cache": "int8 codes + fp32 scales" if args.int8 else "fp16",
                    "l2": "inputs larger than L2 (KV cache >= 1 GB per step)",
                    "parallelism": "replicas" if dctx.world > 1 else "single GPU"},
         "roofline": {"bound": bound, "kernel": b.kernel_name(), "achieved": achieved,
@@ -567,7 +574,7 @@ def main():
         "clocks": clk.summary(),
         "device_status": r["status"],
     }
-    if hasattr(b, "graph_setup"):
+    if getattr(b, "graph_setup", None) is not None:
         g_ms = time_graph(b, steps, warmup, dctx)
         line["step_graph"] = {"value": rate(b.units * dctx.world, g_ms / 1e3, b.unit),
                               "unit": b.unit, "ms_per_step": g_ms, "steps": steps,
@@ -580,7 +587,7 @@ def main():
         torch.cuda.empty_cache()
         for name in ("gqa_decode_70b", "ragged_decode", "prefill_13b", "mha_decode_7b:int8",
                      "gqa_decode_70b:int8", "ragged_decode:int8"):
-            if name == args.workload:
+            if name == args.workload + (":int8" if args.int8 else ""):
                 continue
             try:
                 base, _, kind = name.partition(":")
