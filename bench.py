@@ -1,7 +1,7 @@
 """Benchmark of the paged-KV GQA attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-extra]
+                    [--impl ours|reference] [--no-extra] [--int8]
 
 A step is one pass of the hot path over one batch of synthetic input.  For a
 decode workload: RoPE of the new tokens' Q/K + append of their K/V through
@@ -21,8 +21,13 @@ synchronize on each side, CUDA events on the launching stream; the KV cache
 (>= 1 GB) is larger than the 129 MB L2, so nothing is served from L2 across
 steps.  Per-kernel durations of the dominant kernel come from events around
 its launches inside the same timed loop.  `e2e` repeats the step through the
-same C-ABI calls with the step's inputs copied from pinned host memory and
-the output copied back inside the timed region.
+library's calls with the step's inputs copied from pinned host memory (one
+copy of a buffer that holds them all) and the output copied back inside the
+timed region; for fp16 decode the step runs as the captured step graph
+(pa_step_graph_launch), as a serving loop would replay it.
+
+    --int8   decode workloads: the int8 KV cache path (pa_rope_kv_write_i8 +
+             pa_decode_i8) as the timed step.
 
 --impl reference times the CPU oracle (the only implementation the source
 pages define) on a bounded sample of the same workload.  Under torchrun with
@@ -151,6 +156,34 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
+class PackedInputs:
+    """A step's host inputs laid out in one buffer (each array at a 256-byte
+    aligned offset): one pinned host copy, one device copy, and device views
+    that the library calls take.  An end-to-end step then moves its inputs
+    with a single host-to-device copy."""
+
+    def __init__(self, host, dev):
+        import torch
+        self.layout, off = {}, 0
+        arrays = {k: np.ascontiguousarray(v) for k, v in host.items()}
+        for k, a in arrays.items():
+            self.layout[k] = (off, a)
+            off = (off + a.nbytes + 255) // 256 * 256
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        hv = self.host.numpy()
+        for k, (o, a) in self.layout.items():
+            hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+        self.device = self.host.to(dev)
+        self.views = {}
+        for k, (o, a) in self.layout.items():
+            t = torch.from_numpy(a)
+            self.views[k] = self.device[o:o + a.nbytes].view(t.dtype).view(t.shape)
+
+    def upload(self):
+        self.device.copy_(self.host, non_blocking=True)
+
+
 class DecodeBench:
     def __init__(self, name, dev, int8=False):
         import torch
@@ -165,10 +198,10 @@ class DecodeBench:
         if not int8:
             self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
             self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
-        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
         self.host = dict(q=case.q, k=case.k, v=case.v, positions=md["positions"],
                          slots=md["slot_mapping"], bt=case.block_tables, ctx=md["context_lens"])
-        self.d = {k_: t(v_) for k_, v_ in self.host.items()}
+        self.packed = PackedInputs(self.host, dev)
+        self.d = self.packed.views
         self.ws = pa.decode_workspace(len(case.num_cached), wl.n_heads, wl.n_kv_heads,
                                       wl.head_dim, device=dev)
         self.out = torch.empty_like(self.d["q"])
@@ -189,18 +222,30 @@ class DecodeBench:
             ev[1].record()
 
     def e2e_setup(self):
+        """Inputs from pinned host memory (one copy), the step (replayed as
+        the captured step graph where there is one), output back to pinned
+        host memory."""
         torch = self.torch
-        self.pinned = {k_: torch.from_numpy(np.ascontiguousarray(v_)).pin_memory()
-                       for k_, v_ in self.host.items()}
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(v_.numel() * v_.element_size() for v_ in self.pinned.values())
-        return h2d, self.out_host.numel() * self.out_host.element_size()
+        self.e2e_graph = None
+        if getattr(self, "graph_setup", None) is not None:
+            pa, d, wl = self.pa, self.d, self.case.wl
+            self.e2e_graph = pa.StepGraph(d["q"], d["k"], d["v"], d["positions"], d["slots"],
+                                          self.table, self.cache, d["bt"], d["ctx"], self.ws,
+                                          wl.n_kv_heads, out=self.out, status=self.status)
+        return self.packed.nbytes, self.out_host.numel() * self.out_host.element_size()
 
     def e2e_step(self):
-        for k_, v_ in self.pinned.items():
-            self.d[k_].copy_(v_, non_blocking=True)
-        self.step()
+        self.packed.upload()
+        if self.e2e_graph is not None:
+            self.e2e_graph.launch()
+        else:
+            self.step()
         self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_close(self):
+        if self.e2e_graph is not None:
+            self.e2e_graph.close()
 
     def kernel_name(self):
         return "decode_kernel"
@@ -262,11 +307,11 @@ class PrefillBench:
         self.table = pa.rope_table(int(md["max_seqlen_k"]), wl.head_dim, wl.rope_theta)
         self.cache = pa.Cache(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
         self.cache.tensor.copy_(torch.from_numpy(W.initial_cache(case)))
-        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
         self.host = dict(q=case.q, k=case.k, v=case.v, positions=md["positions"],
                          slots=md["slot_mapping"], bt=case.block_tables,
                          cuq=md["cu_seqlens_q"], cuk=md["cu_seqlens_k"])
-        self.d = {k_: t(v_) for k_, v_ in self.host.items()}
+        self.packed = PackedInputs(self.host, dev)
+        self.d = self.packed.views
         self.out = torch.empty_like(self.d["q"])
         self.status = pa.new_status(dev)
         self.units = prefill_flops(case)
@@ -286,17 +331,16 @@ class PrefillBench:
 
     def e2e_setup(self):
         torch = self.torch
-        self.pinned = {k_: torch.from_numpy(np.ascontiguousarray(v_)).pin_memory()
-                       for k_, v_ in self.host.items()}
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(v_.numel() * v_.element_size() for v_ in self.pinned.values())
-        return h2d, self.out_host.numel() * self.out_host.element_size()
+        return self.packed.nbytes, self.out_host.numel() * self.out_host.element_size()
 
     def e2e_step(self):
-        for k_, v_ in self.pinned.items():
-            self.d[k_].copy_(v_, non_blocking=True)
+        self.packed.upload()
         self.step()
         self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_close(self):
+        pass
 
     def kernel_name(self):
         return "prefill_kernel"
@@ -365,6 +409,7 @@ def time_e2e(b, steps, warmup, dist_ctx):
     stop.record()
     torch.cuda.synchronize()
     dist_ctx.barrier()
+    b.e2e_close()
     return dist_ctx.max(start.elapsed_time(stop) / steps), h2d, d2h
 
 
