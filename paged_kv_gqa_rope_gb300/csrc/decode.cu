@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                 // This lane's codes, read once (the stage is then free again):
                 // K rows head and head + 8, chunks (D/64) quad + m; V tokens
                 // 2 quad + {0, 1, 8, 9}, the D/8 columns from head * D/8.
-                uint32_t kw[2][D / 16], vw[4][D / 32];
+                uint32_t kw[2][D / 16];
                 float ks0 = 0.f, ks1 = 0.f, vs0 = 0.f, vs1 = 0.f;
                 if (!bad) {
 #pragma unroll
@@ -388,33 +388,19 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                             kw[r][4 * m + 3] = x.w ^ 0x80808080u;
                         }
                     }
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int t = 2 * quad + (v & 1) + 8 * (v >> 1);
-                        if constexpr (D == 128) {
-                            const uint4 x = ld_shared_v4(kt + L::kCodeBytes + code_offset<D>(t, head));
-                            vw[v][0] = x.x ^ 0x80808080u;
-                            vw[v][1] = x.y ^ 0x80808080u;
-                            vw[v][2] = x.z ^ 0x80808080u;
-                            vw[v][3] = x.w ^ 0x80808080u;
-                        } else {
-                            const uint2 x = ld_shared_v2(kt + L::kCodeBytes + t * D + head * (D / 8));
-                            vw[v][0] = x.x ^ 0x80808080u;
-                            vw[v][1] = x.y ^ 0x80808080u;
-                        }
-                    }
                     const uint32_t sc = smem_u32(scale_ring + stage * L::kScaleBytes) + head * 4;
                     ks0 = ld_shared_f32(sc);
                     ks1 = ld_shared_f32(sc + 32);
                     vs0 = ld_shared_f32(sc + kBlockSize * 4);
                     vs1 = ld_shared_f32(sc + kBlockSize * 4 + 32);
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    if (bad) stage_bad[stage] = 0;
-                    mbar_arrive(&empty[stage]);
-                }
-                if (!bad) {
+                if (bad) {
+                    __syncwarp();
+                    if (lane == 0) {
+                        stage_bad[stage] = 0;
+                        mbar_arrive(&empty[stage]);
+                    }
+                } else {
                     // S^T on codes + kCodeBias (exact in fp16); the bias adds
                     // kCodeBias * sum(Q) to every score of a column.
                     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -459,6 +445,26 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                     const __half2 p23 = __floats2half2_rn(e2 * vs1, e3 * vs1);
                     const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p01));
                     const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&p23));
+                    // V codes only now (fewer registers live at once), then
+                    // the stage is free again
+                    uint32_t vw[4][D / 32];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int t = 2 * quad + (v & 1) + 8 * (v >> 1);
+                        if constexpr (D == 128) {
+                            const uint4 x = ld_shared_v4(kt + L::kCodeBytes + code_offset<D>(t, head));
+                            vw[v][0] = x.x ^ 0x80808080u;
+                            vw[v][1] = x.y ^ 0x80808080u;
+                            vw[v][2] = x.z ^ 0x80808080u;
+                            vw[v][3] = x.w ^ 0x80808080u;
+                        } else {
+                            const uint2 x = ld_shared_v2(kt + L::kCodeBytes + t * D + head * (D / 8));
+                            vw[v][0] = x.x ^ 0x80808080u;
+                            vw[v][1] = x.y ^ 0x80808080u;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);
                     const float c0 = -kCodeBias * pl0 * al0, c1 = -kCodeBias * pl1 * al1;
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
