@@ -253,7 +253,7 @@ int pa_decode(const void *q, const pa_cache_t *cache, int layer, const int32_t *
  * Returns PA_ERR_WORKSPACE when num_seqs * n_kv_heads is too large for the
  * array (pa_decode_workspace_bytes(...) > PA_DECODE_NOALLOC_SCRATCH_BYTES).
  */
-#define PA_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,

@@ -44,7 +44,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSeqs = 4096;
 constexpr int kGroupPad = 8;   // MMA N: Q heads per KV head, padded
-constexpr int kMaxGrid = 456;  // CTAs the workspace has record slots for (3 per SM)
+constexpr int kMaxGrid = 608;  // CTAs the workspace has record slots for (4 per SM)
 
 struct DecodeArgs {
     const __half *q;              // [B][H][D]
@@ -68,6 +68,9 @@ struct Layout {
     static constexpr int kCodeBytes = kBlockSize * D;      // one int8 K or V block tile
     static constexpr int kStageBytes = I8 ? 2 * kCodeBytes : 2 * kTileBytes;
     static constexpr int kScaleBytes = I8 ? 2 * kBlockSize * 4 : 0;
+    // int8: the segment's Q^T fragments [D/16][32 lanes][2 words], shared by
+    // the consumer warps (read per block instead of held in registers)
+    static constexpr int kQsmBytes = I8 ? (D / 16) * 32 * 8 : 0;
     static constexpr int kRec = D + 4;                     // floats per head record
 };
 
@@ -156,10 +159,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// int8: three CTAs per SM (128 registers): the per-block consumer work, not
-// the bytes in flight, bounds the int8 pipeline, so more consumer warps pay.
+// int8: four CTAs per SM (96 registers; the Q fragments live in shared
+// memory): the per-block consumer work, not the bytes in flight, bounds the
+// int8 pipeline, so more consumer warps pay.
 template <int D, int NSTAGE, bool I8>
-__global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
+__global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap,
                   const __grid_constant__ CUtensorMap smap, const DecodeArgs a) {
     // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
@@ -175,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = smem;
     uint8_t *scale_ring = smem + NSTAGE * L::kStageBytes;  // int8: [NSTAGE][K 16, V 16] floats
-    uint64_t *full = reinterpret_cast<uint64_t *>(scale_ring + NSTAGE * L::kScaleBytes);
+    uint8_t *qsm = scale_ring + NSTAGE * L::kScaleBytes;      // int8: Q^T fragments
+    uint64_t *full = reinterpret_cast<uint64_t *>(qsm + L::kQsmBytes);
     uint64_t *empty = full + NSTAGE;
     int *stage_bad = reinterpret_cast<int *>(empty + NSTAGE);
     float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
@@ -328,8 +333,10 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                         const int d = 16 * ((D / 64) * quad + m) + 4 * i;
                         const uint2 w = hv ? __ldg(reinterpret_cast<const uint2 *>(qrow) + d / 4)
                                            : make_uint2(0u, 0u);
-                        qb[4 * m + i][0] = __byte_perm(w.x, w.y, 0x5410);  // Q[d], Q[d + 2]
-                        qb[4 * m + i][1] = __byte_perm(w.x, w.y, 0x7632);  // Q[d + 1], Q[d + 3]
+                        // Q[d], Q[d + 2] and Q[d + 1], Q[d + 3]; every consumer
+                        // warp writes the same values, so no warp waits for another
+                        st_shared_v2(smem_u32(qsm) + ((4 * m + i) * 32 + lane) * 8,
+                                     __byte_perm(w.x, w.y, 0x5410), __byte_perm(w.x, w.y, 0x7632));
                         const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
                         const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
                         part += (f0.x + f0.y) + (f1.x + f1.y);
@@ -339,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                 part += __shfl_xor_sync(0xffffffffu, part, 2);  // lanes 4h .. 4h+3: head h
                 qbias0 = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * quad);
                 qbias1 = kCodeBias * __shfl_sync(0xffffffffu, part, 8 * quad + 4);
+                __syncwarp();
             } else {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -410,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
                                                 __byte_perm(kw[1][kk], 0x64u, 0x4240),
                                                 __byte_perm(kw[0][kk], 0x64u, 0x4341),
                                                 __byte_perm(kw[1][kk], 0x64u, 0x4341)};
-                        mma_16816(sc, af, qb[kk][0], qb[kk][1]);
+                        const uint2 qf = ld_shared_v2(smem_u32(qsm) + (kk * 32 + lane) * 8);
+                        mma_16816(sc, af, qf.x, qf.y);
                     }
                     float x0 = (sc[0] - qbias0) * (ks0 * a.scale_log2);
                     float x1 = (sc[1] - qbias1) * (ks0 * a.scale_log2);
@@ -734,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, I8 ? 3 : 1)
 template <int D, int NSTAGE, bool I8>
 size_t decode_smem_bytes(int B) {
     return 1024 + (size_t)NSTAGE * Layout<D, I8>::kStageBytes +
-           (size_t)NSTAGE * Layout<D, I8>::kScaleBytes + 2 * NSTAGE * sizeof(uint64_t) +
+           (size_t)NSTAGE * Layout<D, I8>::kScaleBytes + Layout<D, I8>::kQsmBytes +
+           2 * NSTAGE * sizeof(uint64_t) +
            NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
            4 * sizeof(int) + 8 + (size_t)(B + 1) * sizeof(int64_t);
 }
@@ -788,8 +798,8 @@ int launch_decode(const CUtensorMap &map, const DecodeArgs &a, int max_grid, cud
     return launch_decode_stages<D, kStages, false>(map, map, a, max_grid, st);
 }
 
-// int8 cache: a stage holds half the bytes; 12 stages at three CTAs per SM.
-constexpr int kStagesI8 = 12;
+// int8 cache: a stage holds half the bytes; 8 stages at four CTAs per SM.
+constexpr int kStagesI8 = 8;
 
 size_t counters_bytes(int B, int Hk) {
     return ((size_t)B * Hk * sizeof(int32_t) + 255) & ~(size_t)255;

@@ -158,7 +158,7 @@ def test_decode_narrow_grid_merges_pieces(ctxs, Hk, ctas):
     full = pa.decode_workspace_bytes(len(ctxs), H, Hk, d)
     slot_bytes = 2 * 8 * (d + 4) * 4
     counters = (len(ctxs) * Hk * 4 + 255) // 256 * 256
-    assert full == counters + 456 * slot_bytes  # record slots for 3 CTAs per SM
+    assert full == counters + 608 * slot_bytes  # record slots for 4 CTAs per SM
     run.ws = pa.decode_workspace(len(ctxs), H, Hk, d, nbytes=counters + ctas * slot_bytes)
     out = run.run()
     _, _, _, want = oracle_decode_step(case, init)

@@ -71,7 +71,7 @@ def test_decode_noalloc_rejects_too_large(libpa):
     run = DecodeRun(case, init)
     wl = case.wl
     too_many = 4096
-    assert pa.decode_workspace_bytes(too_many, 512, 256, 128) > (4 << 20)
+    assert pa.decode_workspace_bytes(too_many, 512, 256, 128) > (8 << 20)
     rc = libpa.pa_decode_noalloc(
         ctypes.c_void_p(run.q.data_ptr()), ctypes.byref(run.cache.desc), 0,
         ctypes.c_void_p(run.bt.data_ptr()), run.bt.shape[1], ctypes.c_void_p(run.ctx.data_ptr()),
