@@ -16,8 +16,9 @@
 // first) and handed out in that order by a global work counter to the CTAs
 // of a persistent grid as they become free, so the CTAs running at any moment
 // work on neighbouring units, mostly of the same heads, and read each K/V
-// tile from L2 rather than each from HBM; the costliest pair of a head goes
-// first and the cheap ones close the list, which evens out the CTAs' ends.
+// tile from L2 rather than each from HBM; the sequences are listed from the
+// costliest to the cheapest and within a head the costliest pair goes first,
+// so the cheap units close the list, which evens out the CTAs' ends.
 //
 // Roles (512 threads):
 //   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
@@ -107,7 +108,8 @@ struct PL {
     static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
     static constexpr int kBar = kV + VS * kKVTile;
     static constexpr int kLsum = kBar + 1024;         // float [2 tiles][2 units][128]: row sums
-    static constexpr int kTab = kLsum + 2048;         // int4 [B + 1]: sequence table
+    static constexpr int kSeqId = kLsum + 2048;       // int [kThreads]: sequence of each table row
+    static constexpr int kTab = kSeqId + 4 * kThreads;  // int4 [B + 1]: sequence table
     static size_t bytes(int B) { return (size_t)kTab + (size_t)(B + 1) * 16; }
     static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
 };
@@ -235,9 +237,11 @@ __device__ __forceinline__ bool seq_ok(const PrefillArgs &a, const SeqInfo &si) 
 // to the first).  CTAs take units from the list in order as they finish
 // others, so the CTAs running at any moment work on neighbouring units,
 // mostly of the same heads, and share those heads' K/V tiles in L2; within a
-// head the costliest pair comes first, so the list ends on cheap units.
-// `tab` is the shared-memory sequence table: tab[s] = {units of sequences
-// before s, q_begin, L_q, k_len}, tab[B].x = all units.
+// head the costliest pair comes first, and the sequences are listed from
+// the costliest to the cheapest (batches of up to kThreads sequences), so
+// the list ends on cheap units.  `tab` is the shared-memory sequence table:
+// tab[i] = {units of rows before i, q_begin, L_q, k_len} of sequence
+// seqid[i] (i itself when seqid is null), tab[B].x = all units.
 struct UnitIter {
     int u;  // unit index
     int s, h, k;
@@ -246,7 +250,7 @@ struct UnitIter {
     PairShape ps;
 
     // Unit idx from the sequence table (the scheduler decodes each unit once).
-    __device__ __forceinline__ void decode(int B, const int4 *tab, int idx) {
+    __device__ __forceinline__ void decode(int B, const int4 *tab, const int *seqid, int idx) {
         u = idx;
         if (u >= tab[B].x) return;
         int lo = 0, hi = B - 1;  // largest s with tab[s].x <= u
@@ -257,8 +261,8 @@ struct UnitIter {
             else
                 hi = mid - 1;
         }
-        s = lo;
-        const int4 e = tab[s];
+        const int4 e = tab[lo];
+        s = seqid ? seqid[lo] : lo;
         si.q_begin = e.y;
         si.L_q = e.z;
         si.k_len = e.w;
@@ -329,6 +333,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) tab[0].x = 0;
     __syncthreads();
+    // ---- sequences from the costliest (visible query-key pairs) to the
+    // cheapest: rank by counting, one sequence per thread
+    int *seqid = reinterpret_cast<int *>(smem + L::kSeqId);
+    const bool ranked = B <= kThreads;
+    if (ranked) {
+        int4 mine = make_int4(0, 0, 0, 0);
+        int rank = 0;
+        if (tid < B) {
+            mine = make_int4(tab[tid + 1].x, tab[tid].y, tab[tid].z, tab[tid].w);
+            auto cost = [](int units, int L_q, int k_len) -> long long {
+                return units > 0 ? (long long)L_q * (2ll * k_len - L_q) : 0ll;
+            };
+            const long long c = cost(mine.x, mine.z, mine.w);
+            for (int o = 0; o < B; ++o) {
+                const long long co = cost(tab[o + 1].x, tab[o].z, tab[o].w);
+                rank += (co > c || (co == c && o < tid)) ? 1 : 0;
+            }
+        }
+        __syncthreads();
+        if (tid < B) {
+            tab[rank].y = mine.y;
+            tab[rank].z = mine.z;
+            tab[rank].w = mine.w;
+            tab[rank + 1].x = mine.x;
+            seqid[rank] = tid;
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         int carry = 0;
         for (int base = 1; base <= B; base += 32) {
@@ -349,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total_units = tab[B].x;
     if (tid == 0) {
         UnitIter u0;
-        u0.decode(B, tab, min(atomicAdd(&g_sched_next[a.sched], 1), total_units));
+        u0.decode(B, tab, ranked ? seqid : nullptr,
+                  min(atomicAdd(&g_sched_next[a.sched], 1), total_units));
         u0.store(uring);
     }
     __syncthreads();
@@ -733,8 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(&bar[B_KSTART], (i - 1) & 1);
                 if (ok && i >= kRing) ok = mbar_wait(&bar[B_UEMPTY + slot], ((i / kRing) - 1) & 1);
                 UnitIter u;
-                u.decode(B, tab, ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units)
-                                    : total_units);
+                u.decode(B, tab, ranked ? seqid : nullptr,
+                         ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units) : total_units);
                 u.store(uring + 2 * slot);
                 mbar_arrive(&bar[B_UFULL + slot]);
                 if (u.u >= total_units) break;
