@@ -616,6 +616,13 @@ def main():
         "e2e": {"value": rate(b.units * dctx.world, e2e_ms / 1e3, b.unit), "unit": b.unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": b.launches_per_step * steps,
+        # (tensor-bound lines) the same against the sustained cuBLAS figure,
+        # which was measured with the clocks held down by the power cap
+        **({"roofline_sustained": {"peak": peaks[2], "frac": achieved / peaks[2],
+                                   "note": "peak of a seconds-long cuBLAS loop at "
+                                           "power-capped clocks; this kernel runs at "
+                                           "the clocks in 'clocks'"}}
+           if b.unit != "GB/s" and peaks[2] else {}),
         "clocks": clk.summary(),
         "device_status": r["status"],
     }
@@ -646,6 +653,8 @@ def main():
                                "kernel": eb.kernel_name(), "kernel_ms": er["kernel_ms"],
                                "kernel_achieved": ach, "frac_of_peak": ach / pk,
                                "steps": n, "device_status": er["status"]}
+                if eb.unit != "GB/s" and peaks[2]:
+                    extra[name]["frac_of_sustained_peak"] = ach / peaks[2]
                 del eb
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep the headline

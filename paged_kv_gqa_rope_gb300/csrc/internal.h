@@ -74,6 +74,16 @@ EncodeTiledFn encode_tiled();
 // with a box of {64, box_halves, 1, box_rows, 1} and 128-byte swizzle.
 // Plane index of (kv, layer) is kv * layers + layer.  Returns false on error.
 bool make_cache_map(CUtensorMap *map, const pa_cache_t *c, int box_halves, int box_rows);
+
+// Grid of the per-token kernels (RoPE/append): x = chunks of kTokenThreads
+// pieces of one token, y (and z past 65535 tokens) = token.
+constexpr int kTokenThreads = 256;
+inline dim3 token_grid(int num_tokens, int pieces_per_token) {
+    const unsigned chunks = (unsigned)((pieces_per_token + kTokenThreads - 1) / kTokenThreads);
+    const unsigned y = (unsigned)(num_tokens < 65535 ? num_tokens : 65535);
+    const unsigned z = (unsigned)((num_tokens + 65534) / 65535);
+    return dim3(chunks, y, z);
+}
 // The same view of one layer with dim4 = its 2 planes (K, V; stride
 // kv_stride) and a box of {64, head_dim / 64, 1, block_size, 2}: a block's
 // whole K tile, then its V tile, in one copy.

@@ -2,10 +2,10 @@
 // cache; the scheme is this library's, see include/pa.h): allocation and
 // the RoPE + append kernel that quantises each appended K/V row.
 //
-// Like rope_kv_write_kernel, one thread handles one 16-byte piece (8 fp16
-// values) of one head row; the D/8 threads of a K or V row (consecutive
-// lanes of one warp) reduce the row's absolute maximum with shuffles, then
-// each writes its 8 codes and the first the row's scale.
+// Like rope_kv_write_kernel (same per-token grid), one thread handles one
+// 16-byte piece (8 fp16 values) of one head row; the D/8 threads of a K or V
+// row (consecutive lanes of one warp) reduce the row's absolute maximum with
+// shuffles, then each writes its 8 codes and the first the row's scale.
 #include <string.h>
 
 #include "common.cuh"
@@ -42,15 +42,15 @@ __global__ void __launch_bounds__(256) rope_kv_write_i8_kernel(const RopeI8Args 
     griddep_launch_dependents();
     constexpr int kPieces = D / 8;  // 16-byte pieces per head row (a power of two <= 16)
     const int rows = a.n_heads + 2 * a.n_kv_heads;
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t total = (int64_t)a.num_tokens * rows * kPieces;
-    // Threads past the end (whole rows of them) still take part in the row
-    // reductions below; they read token 0 and write nothing.
-    const bool live = idx < total;
-    const int64_t i = live ? idx : idx % kPieces;
-    const int piece = (int)(i % kPieces);
-    const int row = (int)((i / kPieces) % rows);
-    const int t = (int)(i / ((int64_t)kPieces * rows));
+    const int t = (int)(blockIdx.z * gridDim.y + blockIdx.y);
+    if (t >= a.num_tokens) return;  // the whole CTA
+    const int idx = (int)(blockIdx.x * blockDim.x + threadIdx.x);  // piece within the token
+    // Threads past the token's last row (whole rows of them) still take part
+    // in the row reductions below; they read row 0 and write nothing.
+    const bool live = idx < rows * kPieces;
+    const int i = live ? idx : idx % kPieces;
+    const int piece = i % kPieces;
+    const int row = i / kPieces;
 
     const int pos = __ldg(a.positions + t);
     const bool pos_ok = pos >= 0 && pos < a.max_pos;
@@ -211,13 +211,11 @@ extern "C" int pa_rope_kv_write_i8(void *q, void *k, const void *v, const int32_
     a.n_kv_heads = n_kv_heads;
     a.max_pos = max_positions;
 
-    const int64_t total = (int64_t)num_tokens * (n_heads + 2 * n_kv_heads) * (head_dim / 8);
-    const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
+    const dim3 grid = token_grid(num_tokens, (n_heads + 2 * n_kv_heads) * (head_dim / 8));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (head_dim == 128)
-        rope_kv_write_i8_kernel<128><<<(unsigned)blocks, threads, 0, st>>>(a);
+        rope_kv_write_i8_kernel<128><<<grid, kTokenThreads, 0, st>>>(a);
     else
-        rope_kv_write_i8_kernel<64><<<(unsigned)blocks, threads, 0, st>>>(a);
+        rope_kv_write_i8_kernel<64><<<grid, kTokenThreads, 0, st>>>(a);
     return launch_status();
 }

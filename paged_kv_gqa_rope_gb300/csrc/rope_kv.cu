@@ -6,8 +6,12 @@
 // One thread moves one 16-byte piece (8 fp16 = 4 rotation pairs) of one head
 // row.  A token has n_heads Q rows, n_kv_heads K rows and n_kv_heads V rows;
 // consecutive threads take consecutive pieces, so every warp reads and writes
-// whole 128-byte lines.  The kernel is bound by HBM: it reads Q, K and V once
-// and writes Q, K, cache K and cache V once.
+// whole 128-byte lines.  The grid has one row of CTAs per token (blockIdx.y,
+// and blockIdx.z past 65535 tokens), each CTA 256 pieces of it, so the row
+// and piece of a thread come from shifts, not divisions (one piece per
+// thread measured faster than two or four with their loads issued first).  The kernel is
+// bound by HBM: it reads Q, K and V once and writes Q, K, cache K and cache
+// V once.
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,18 +33,17 @@ struct RopeArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
+__global__ void __launch_bounds__(kTokenThreads) rope_kv_write_kernel(const RopeArgs a) {
     // The decode or prefill kernel that follows may start its set-up now; it
     // waits (griddepcontrol.wait) for this kernel's writes before using them.
     griddep_launch_dependents();
     constexpr int kPieces = D / 8;  // 16-byte pieces per head row
     const int rows = a.n_heads + 2 * a.n_kv_heads;
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t total = (int64_t)a.num_tokens * rows * kPieces;
-    if (idx >= total) return;
-    const int piece = (int)(idx % kPieces);
-    const int row = (int)((idx / kPieces) % rows);
-    const int t = (int)(idx / ((int64_t)kPieces * rows));
+    const int t = (int)(blockIdx.z * gridDim.y + blockIdx.y);
+    const int i = (int)(blockIdx.x * blockDim.x + threadIdx.x);  // piece within the token
+    if (t >= a.num_tokens || i >= rows * kPieces) return;
+    const int piece = i % kPieces;
+    const int row = i / kPieces;
 
     const int pos = __ldg(a.positions + t);
     if (pos < 0 || pos >= a.max_pos) {
@@ -112,13 +115,11 @@ extern "C" int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *
     a.n_kv_heads = n_kv_heads;
     a.max_pos = max_positions;
 
-    const int64_t total = (int64_t)num_tokens * (n_heads + 2 * n_kv_heads) * (head_dim / 8);
-    const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
+    const dim3 grid = token_grid(num_tokens, (n_heads + 2 * n_kv_heads) * (head_dim / 8));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (head_dim == 128)
-        rope_kv_write_kernel<128><<<(unsigned)blocks, threads, 0, st>>>(a);
+        rope_kv_write_kernel<128><<<grid, kTokenThreads, 0, st>>>(a);
     else
-        rope_kv_write_kernel<64><<<(unsigned)blocks, threads, 0, st>>>(a);
+        rope_kv_write_kernel<64><<<grid, kTokenThreads, 0, st>>>(a);
     return launch_status();
 }
