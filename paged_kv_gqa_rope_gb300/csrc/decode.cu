@@ -17,8 +17,9 @@
 // softmax and resets the pair's arrival counter to zero.
 //
 // Inside a CTA one producer warp streams the K and V block tiles (16 tokens x
-// head_dim fp16 of one KV head) with TMA into a ring of shared-memory stages;
-// four consumer warps take the blocks of a segment in turn.  Each warp
+// head_dim fp16 of one KV head; one TMA copy brings both) into a ring of
+// shared-memory stages; four consumer warps take the blocks of a segment in
+// turn (two CTAs per SM for the fp16 cache).  Each warp
 // computes, with warp-level tensor-core MMAs,
 //     S^T (16 tokens x 8 heads) = K (16 x d) . Q^T (d x 8 heads)
 // so the g Q heads that share the KV head form the N = 8 dimension and each
@@ -29,6 +30,11 @@
 //     O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads).
 // The four warps' (max, sum, O) are merged through shared memory at the end
 // of each segment.
+//
+// The int8 cache (pa_decode_i8) runs the same kernel with I8 = true: the
+// stages hold code tiles and scales, and each consumer warp builds the MMA
+// fragments from the codes in registers (see the int8 branch below); four
+// CTAs per SM.
 //
 // Bound: HBM.  Algorithmic bytes = sum_s context_lens[s] * Hk * d * 2 (K, V)
 // * 2 B; everything else (Q, O, tables, partial records) is < 0.5 % of it.
