@@ -186,6 +186,17 @@ def test_prefill_many_sequences():
     check(case, init)
 
 
+def test_prefill_more_sequences_than_threads():
+    """Past 512 sequences the kernel keeps the batch order instead of ranking
+    the sequences by cost in its prologue (one sequence per thread)."""
+    rng = np.random.default_rng(43)
+    B = 700
+    cached = rng.integers(0, 40, size=B).tolist()
+    new = rng.integers(1, 24, size=B).tolist()
+    case, init = custom_prefill_case(4, 2, 64, cached, new, seed=44)
+    check(case, init)
+
+
 def test_prefill_rising_maximum_rescales():
     """Keys whose norm grows with their position make later key tiles, and the
     second half of a tile, raise a row's running maximum past the rescale
