@@ -812,12 +812,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // first tile) scales the first half's P, already in TMEM.
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
+                    // The TMEM load returns each 32 columns' maximum too
+                    // (tcgen05.ld.red); a masked tile takes it after masking.
                     uint32_t sa[32], sb[32];
-                    tc::ld32_issue(s_tmem + hf * 64, sa);
-                    tc::ld32_issue(s_tmem + hf * 64 + 32, sb);
-                    tc::wait_ld(sa, sb);
-                    if (masked) mask_cols(sa, sb, hf * 64, kl);
-                    const float m_t = half_max(sa, sb) * sl2;
+                    float ma, mb;
+                    tc::ld32_max_issue(s_tmem + hf * 64, sa, ma);
+                    tc::ld32_max_issue(s_tmem + hf * 64 + 32, sb, mb);
+                    tc::wait_ld(sa, sb, ma, mb);
+                    float mx = fmaxf(ma, mb);
+                    if (masked) {
+                        mask_cols(sa, sb, hf * 64, kl);
+                        mx = half_max(sa, sb);
+                    }
+                    const float m_t = mx * sl2;
                     const bool up = m_t > m_used + kRescaleThreshold;
                     float a = 1.f;
                     if (up) {

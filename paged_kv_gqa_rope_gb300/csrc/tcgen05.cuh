@@ -130,6 +130,20 @@ __device__ __forceinline__ void ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// The same load with the maximum over the 32 loaded columns of this lane
+// (tcgen05.ld.red, sm_103a): `m` is valid after wait_ld() like the values.
+__device__ __forceinline__ void ld32_max_issue(uint32_t taddr, uint32_t (&r)[32], float &m) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=f"(m)
+        : "r"(taddr)
+        : "memory");
+}
+
 // Wait for this thread's outstanding TMEM loads.  The two register sets are
 // passed through so no use of them can be scheduled before the wait.
 __device__ __forceinline__ void wait_ld(uint32_t (&a)[32], uint32_t (&b)[32]) {
@@ -144,6 +158,13 @@ __device__ __forceinline__ void wait_ld(uint32_t (&a)[32], uint32_t (&b)[32]) {
           "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
         :
         : "memory");
+}
+
+// wait_ld for two loads with maxima (ld32_max_issue).
+__device__ __forceinline__ void wait_ld(uint32_t (&a)[32], uint32_t (&b)[32], float &ma,
+                                        float &mb) {
+    wait_ld(a, b);
+    asm volatile("" : "+f"(ma), "+f"(mb) : : "memory");
 }
 
 // Store 16 consecutive 32-bit columns of this thread's lane (32x32b, x16).
