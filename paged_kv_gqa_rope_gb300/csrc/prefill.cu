@@ -134,7 +134,9 @@ enum {
     B_UFULL = 30,   // kRing: unit ring entry written
     B_UEMPTY = 38,  // kRing: entry read by every consumer warp
     B_KSTART = 46,  // the K producer started a unit
-    B_COUNT = 47
+    B_PHALF = 47,   // per query tile: P of the score tile's first 64 keys written
+    B_OHALF = 49,   // per query tile: the P.V of those 64 keys done
+    B_COUNT = 51
 };
 static_assert(B_COUNT * 8 + 4 <= kRingByte && kRingByte + kRing * 32 <= 1024, "barrier area");
 
@@ -406,6 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_QEMPTY + i], 1);
             mbar_init(&bar[B_SFULL + i], 1);
             mbar_init(&bar[B_PREADY + i], 128);
+            mbar_init(&bar[B_PHALF + i], 128);
+            mbar_init(&bar[B_OHALF + i], 1);
             mbar_init(&bar[B_ODONE + i], 1);
             mbar_init(&bar[B_OFREE + i], 128);
             mbar_init(&bar[B_LREADY + 2 * i], 128);
@@ -718,16 +722,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < 2; ++t) {
                         if (!ok || j >= u.ps.n[t]) continue;
                         const int G = gt[t] + j;
-                        ok = mbar_wait(&bar[B_PREADY + t], G & 1);
+                        // P.V in two halves of 64 keys: the first as soon as
+                        // the softmax has written P for them, the second when
+                        // the whole tile's P is in TMEM.
+                        ok = mbar_wait(&bar[B_PHALF + t], G & 1);
                         if (ok && j == 0 && units_t[t] > 0)
                             ok = mbar_wait(&bar[B_OFREE + t], (units_t[t] - 1) & 1);
                         tc::fence_after();
                         if (!ok) continue;
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk)
+                        for (int kk = 0; kk < kBN / 32; ++kk)
                             tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t) + kk * 8,
                                        dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        tc::commit(&bar[B_OHALF + t]);
+                        ok = mbar_wait(&bar[B_PREADY + t], G & 1);
+                        tc::fence_after();
+                        if (!ok) continue;
+#pragma unroll
+                        for (int kk = kBN / 32; kk < kBN / 16; ++kk)
+                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t) + kk * 8,
+                                       dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
                         tc::commit(&bar[B_ODONE + t]);
                         if (t == t_last) tc::commit(&bar[B_VEMPTY + st]);  // V_j free
                         if (j + 1 < u.ps.n[t]) {
@@ -803,13 +818,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool masked = j * kBN + kBN - 1 > first_row;
                 const int kl = key_lim - j * kBN;  // last visible column of this tile
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                float alpha = 1.f;     // factor on O (and on l) for this tile
-                bool raised = false;   // the row's running maximum moved
-                uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
-                // Each 64-column half is read from TMEM once: its maximum
-                // (from the registers), then P over S.  A second half that
-                // raises the maximum past the threshold (rare after a row's
-                // first tile) scales the first half's P, already in TMEM.
+                // Each 64-column half is read from TMEM once: its maximum, then
+                // P over S; then the half goes to the P.V (keys 0-63 on
+                // B_PHALF, the rest on B_PREADY), so the tensor core starts on
+                // the first half while the second is computed.  A half that
+                // raises the running maximum past the threshold (rare after a
+                // row's first tile) first scales O_t down to it: O_t then holds
+                // the earlier tiles' P.V, and for the second half also this
+                // tile's first-half P.V, made with the old maximum.
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
                     // The TMEM load returns each 32 columns' maximum too
@@ -831,57 +847,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a = ex2(m_used - m_t);  // 0 on the first tile
                         l *= a;
                         m_used = m_t;
-                        alpha *= a;
-                        raised = true;
+                    }
+                    if ((j > 0 || hf == 1) && __any_sync(0xffffffffu, up)) {
+                        // O_t must hold the P.V it is scaled with (normally
+                        // complete: the previous tile's was issued before S_t).
+                        ok = __all_sync(0xffffffffu,
+                                        hf == 0 ? mbar_wait(&bar[B_ODONE + t], (G - 1) & 1)
+                                                : mbar_wait(&bar[B_OHALF + t], G & 1));
+                        if (!ok) break;
+                        tc::fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t orr[32];
+                            tc::ld32(o_tmem + c * 32, orr);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * a);
+                            tc::st32(o_tmem + c * 32, orr);
+                        }
                     }
                     {
+                        uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
                         uint32_t pa[16], pb[16];
                         exp_half(sa, sb, sl2x2, m_used, pa, pb, la, lb);
                         tc::st16(s_tmem + hf * 32, pa);
                         tc::st16(s_tmem + hf * 32 + 16, pb);
-                    }
-                    if (hf == 0) {  // the first half's sum joins l (scaled with it)
                         float x0, x1, y0, y1;
                         f2_unpack(la, x0, x1);
                         f2_unpack(lb, y0, y1);
                         l += (x0 + x1) + (y0 + y1);
-                        la = lb = 0;
-                    } else if (__any_sync(0xffffffffu, up)) {
-                        tc::wait_st();
-                        uint32_t p0[32];
-                        tc::ld32(s_tmem, p0);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&p0[i]));
-                            p0[i] = pack_half2(f.x * a, f.y * a);
-                        }
-                        tc::st32(s_tmem, p0);
                     }
+                    tc::wait_st();
+                    tc::fence_before();
+                    mbar_arrive(&bar[hf == 0 ? B_PHALF + t : B_PREADY + t]);
                 }
-                if (j > 0 && __any_sync(0xffffffffu, raised)) {
-                    // O_t must hold the previous tile's P.V before it is scaled
-                    // (normally complete: S_t was issued behind it).
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ODONE + t], (G - 1) & 1));
-                    if (!ok) break;
-                    tc::fence_after();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t orr[32];
-                        tc::ld32(o_tmem + c * 32, orr);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * alpha);
-                        tc::st32(o_tmem + c * 32, orr);
-                    }
-                }
-                {
-                    float x0, x1, y0, y1;
-                    f2_unpack(la, x0, x1);
-                    f2_unpack(lb, y0, y1);
-                    l += (x0 + x1) + (y0 + y1);
-                }
-                tc::wait_st();
-                tc::fence_before();
-                mbar_arrive(&bar[B_PREADY + t]);
+                if (!ok) break;
             }
             if (!ok) break;
             // The row sum goes to the output warpgroup, which waits for the
