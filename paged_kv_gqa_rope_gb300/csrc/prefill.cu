@@ -41,12 +41,15 @@
 //                       read P0 before S0 is written; no wait in between)
 //   O1 += P1 . V_j,  S1 = Q1 . K_j+1^T
 // so softmax_0 works on S0(j+1) while the tensor core runs tile 1's MMAs and
-// softmax_1 while it runs tile 0's.  Every MMA has N = 128 (M = 128, K = 16):
-// a tcgen05.mma takes about 96 cycles at any N up to 128, so wide tiles use
-// the tensor core better.  The running maximum only moves when a tile raises
-// it by more than 8 (log2 units), so P <= 256 and O is rescaled (in TMEM)
-// only on those tiles.  The row sum adds P in fp32 before its rounding to
-// fp16 (the two differ by far less than the output's own fp16 rounding).
+// softmax_1 while it runs tile 0's.  Each P_t.V_j runs in two halves of 64
+// keys: the first as soon as the softmax has written P for them, the second
+// once the whole tile's P is written.  Every MMA has N = 128 (M = 128,
+// K = 16): a tcgen05.mma takes about 96 cycles at any N up to 128, so wide
+// tiles use the tensor core better.  The running maximum only moves when a
+// half tile raises it by more than 8 (log2 units), so P <= 256 and O is
+// rescaled (in TMEM) only then.  The row sum adds P in fp32 before its
+// rounding to fp16 (the two differ by far less than the output's own fp16
+// rounding).
 //
 // Bound: tensor cores.  Algorithmic FLOPs = 4 * d * H * (number of visible
 // (query, key) pairs).
