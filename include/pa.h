@@ -114,7 +114,9 @@ int pa_free_cache(pa_cache_t *cache);
  *   cu_seqlens_k   host int32 [num_seqs + 1]         (output; seqlen_k = cached + new)
  *   max_seqlen_q/k host int32 scalars               (output, may be NULL)
  * Returns PA_ERR_INVALID for negative lengths, a block table row too short
- * for its sequence, or a negative block id on a needed entry.
+ * for its sequence, a needed entry that is negative or whose slots pass
+ * INT32_MAX, or totals (sum num_new, sum cached + new) past INT32_MAX.
+ * Nothing is written on error.
  */
 int pa_prepare_prefill(int num_seqs, const int32_t *num_cached, const int32_t *num_new,
                        const int32_t *block_tables, int max_blocks_per_seq, int block_size,
@@ -127,6 +129,9 @@ int pa_prepare_prefill(int num_seqs, const int32_t *num_cached, const int32_t *n
  * K/V goes to that position's slot; afterwards context_lens[s] =
  * num_cached[s] + 1 (the page's example: positions [5,3], context_lens [6,4]).
  *   positions, slot_mapping, context_lens   host int32 [num_seqs] (output)
+ * Returns PA_ERR_INVALID for a negative num_cached, a block table row too
+ * short for its position, or a needed entry that is negative or whose slots
+ * pass INT32_MAX.  Nothing is written on error.
  */
 int pa_prepare_decode(int num_seqs, const int32_t *num_cached, const int32_t *block_tables,
                       int max_blocks_per_seq, int block_size, int32_t *positions,

@@ -46,7 +46,9 @@ extern "C" {
 
 typedef struct pa_block_manager *pa_bm_t;
 
-/* A manager of num_blocks blocks of block_size tokens; NULL on bad sizes. */
+/* A manager of num_blocks blocks of block_size tokens; NULL on bad sizes
+ * (either not positive, or num_blocks * block_size past INT32_MAX: slot ids
+ * are int32). */
 pa_bm_t pa_bm_create(int num_blocks, int block_size);
 void pa_bm_destroy(pa_bm_t bm);
 

@@ -113,6 +113,7 @@ extern "C" {
 
 pa_bm_t pa_bm_create(int num_blocks, int block_size) {
     if (num_blocks <= 0 || block_size <= 0) return nullptr;
+    if ((int64_t)num_blocks * block_size > INT32_MAX) return nullptr;  // slots are int32
     pa_block_manager *bm = new (std::nothrow) pa_block_manager;
     if (!bm) return nullptr;
     bm->nb = num_blocks;
@@ -186,7 +187,7 @@ int pa_bm_next_chunk(pa_bm_t bm, int64_t seq_id, int max_tokens, int *num_cached
 
 int pa_bm_mark_computed(pa_bm_t bm, int64_t seq_id, int num_tokens) {
     Seq *s = bm ? bm->find(seq_id) : nullptr;
-    if (!s || num_tokens < 0 || s->computed + num_tokens > (int)s->tokens.size())
+    if (!s || num_tokens < 0 || num_tokens > (int)s->tokens.size() - s->computed)
         return PA_ERR_INVALID;
     s->computed += num_tokens;
     return PA_OK;

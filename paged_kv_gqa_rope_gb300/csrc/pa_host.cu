@@ -79,6 +79,15 @@ bool make_cache_pair_map(CUtensorMap *map, const pa_cache_t *c, int layer) {
 
 using namespace pa;
 
+namespace {
+
+// A block id whose slots block * block_size .. + block_size - 1 are int32.
+bool slot_fits(int32_t block, int block_size) {
+    return block >= 0 && ((int64_t)block + 1) * block_size - 1 <= INT32_MAX;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t pa_cache_bytes(int layers, int num_blocks, int block_size, int n_kv_heads, int head_dim) {
@@ -132,7 +141,7 @@ int pa_prepare_prefill(int num_seqs, const int32_t *num_cached, const int32_t *n
                          !cu_seqlens_k))
         return PA_ERR_INVALID;
     // First pass: validate everything before writing any output.
-    int64_t total = 0;
+    int64_t total = 0, total_k = 0;
     for (int s = 0; s < num_seqs; ++s) {
         const int64_t start = num_cached[s], n = num_new[s];
         if (start < 0 || n < 0) return PA_ERR_INVALID;
@@ -140,14 +149,16 @@ int pa_prepare_prefill(int num_seqs, const int32_t *num_cached, const int32_t *n
         if (end > INT32_MAX) return PA_ERR_INVALID;
         if (n > 0 && (end - 1) / block_size >= max_blocks_per_seq) return PA_ERR_INVALID;
         total += n;
-        if (total > INT32_MAX) return PA_ERR_INVALID;
+        total_k += end;  // cu_seqlens_k is int32 too
+        if (total > INT32_MAX || total_k > INT32_MAX) return PA_ERR_INVALID;
         for (int64_t lb = start / block_size; n > 0 && lb <= (end - 1) / block_size; ++lb)
-            if (block_tables[(int64_t)s * max_blocks_per_seq + lb] < 0) return PA_ERR_INVALID;
+            if (!slot_fits(block_tables[(int64_t)s * max_blocks_per_seq + lb], block_size))
+                return PA_ERR_INVALID;
     }
     if (total > 0 && (!positions || !slot_mapping)) return PA_ERR_INVALID;
     int32_t mq = 0, mk = 0, t = 0;
-    cu_seqlens_q[0] = 0;
-    cu_seqlens_k[0] = 0;
+    if (cu_seqlens_q) cu_seqlens_q[0] = 0;  // both may be NULL when num_seqs == 0
+    if (cu_seqlens_k) cu_seqlens_k[0] = 0;
     for (int s = 0; s < num_seqs; ++s) {
         const int32_t start = num_cached[s], n = num_new[s], end = start + n;
         const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
@@ -175,7 +186,7 @@ int pa_prepare_decode(int num_seqs, const int32_t *num_cached, const int32_t *bl
     for (int s = 0; s < num_seqs; ++s) {
         const int64_t p = num_cached[s];
         if (p < 0 || p >= INT32_MAX || p / block_size >= max_blocks_per_seq) return PA_ERR_INVALID;
-        if (block_tables[(int64_t)s * max_blocks_per_seq + p / block_size] < 0)
+        if (!slot_fits(block_tables[(int64_t)s * max_blocks_per_seq + p / block_size], block_size))
             return PA_ERR_INVALID;
     }
     for (int s = 0; s < num_seqs; ++s) {

@@ -123,3 +123,44 @@ def test_step_graph_rejects_null_handles(libpa):
     assert libpa.pa_step_graph_destroy(None) == pa.PA_ERR_INVALID
     assert libpa.pa_step_graph_create(None, *([None] * 6), 0, None, 0, None, 0, None,
                                       1, 8, 8, 128, 0.0, None, 0, None, None) == pa.PA_ERR_INVALID
+
+
+def _prefill_raw(libpa, num_cached, num_new, table, block_size):
+    nc, nn = (np.ascontiguousarray(x, np.int32) for x in (num_cached, num_new))
+    bt = np.ascontiguousarray(table, np.int32)
+    t = max(int(nn.astype(np.int64).sum()), 1)
+    out = [np.full(t, -7, np.int32), np.full(t, -7, np.int32),
+           np.full(len(nn) + 1, -7, np.int32), np.full(len(nn) + 1, -7, np.int32)]
+    rc = libpa.pa_prepare_prefill(len(nn), pa._p(nc), pa._p(nn), pa._p(bt), bt.shape[1], block_size,
+                                  *(pa._p(a) for a in out), None, None)
+    return rc, out
+
+
+def test_prepare_rejects_int32_overflow(libpa):
+    # Two sequences of ~1.1e9 keys each: each fits int32, cu_seqlens_k's sum
+    # does not.  A block size of 2^28 keeps the tables tiny.
+    bs = 1 << 28
+    table = np.tile(np.arange(8, dtype=np.int32), (2, 1))
+    big = 1_100_000_000
+    rc, out = _prefill_raw(libpa, [big], [1], table[:1], bs)
+    assert rc == pa.PA_OK and out[3].tolist() == [0, big + 1]
+    rc, out = _prefill_raw(libpa, [big, big], [1, 1], table, bs)
+    assert rc == pa.PA_ERR_INVALID
+    assert all((a == -7).all() for a in out)  # nothing written on error
+    # Slots are int32: block id b covers slots b*16 .. b*16+15.
+    last_ok = (2**31 - 1) // 16
+    rc, out = _prefill_raw(libpa, [0], [16], [[last_ok]], 16)
+    assert rc == pa.PA_OK and int(out[1][-1]) == 2**31 - 1
+    rc, _ = _prefill_raw(libpa, [0], [1], [[last_ok + 1]], 16)
+    assert rc == pa.PA_ERR_INVALID
+    with pytest.raises(pa.PAError):
+        pa.prepare_decode([3], np.array([[last_ok + 1]], np.int32))
+    assert pa.prepare_decode([3], np.array([[last_ok]], np.int32))["slot_mapping"].tolist() == [last_ok * 16 + 3]
+
+
+def test_prepare_prefill_no_sequences_accepts_null_outputs(libpa):
+    assert libpa.pa_prepare_prefill(0, None, None, None, 0, 16, None, None, None, None, None,
+                                    None) == pa.PA_OK
+    md = pa.prepare_prefill([], [], np.zeros((0, 1), np.int32))
+    assert md["cu_seqlens_q"].tolist() == [0] and md["cu_seqlens_k"].tolist() == [0]
+    assert md["max_seqlen_q"] == 0 and md["max_seqlen_k"] == 0

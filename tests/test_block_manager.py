@@ -270,3 +270,18 @@ def test_random_operations_match_the_model():
         assert bm.num_free() == len(m.free), step
     for sid in live:
         assert bm.block_table(sid).tolist() == m.seqs[sid][1]
+
+
+def test_create_refuses_pools_past_int32_slots(libpa):
+    with pytest.raises(ValueError):
+        pa.BlockManager(2**27, 16)  # 2^31 slots: their count is past INT32_MAX
+    with pytest.raises(ValueError):
+        pa.BlockManager(0, 16)
+
+
+def test_mark_computed_rejects_overflowing_counts(libpa):
+    bm = pa.BlockManager(8, 16)
+    bm.allocate(1, list(range(20)))
+    with pytest.raises(pa.PAError):
+        bm.mark_computed(1, 2**31 - 1)
+    bm.mark_computed(1, 20)
