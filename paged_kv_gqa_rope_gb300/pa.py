@@ -145,10 +145,32 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t, dtype, name):
+def _dev(t, dtype, name, shape=None):
+    """A contiguous CUDA tensor of `dtype`; with `shape`, of exactly that shape
+    (None entries free).  The library sees only pointers, so the sizes its
+    kernels index by are checked here."""
     if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous()):
         raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    if shape is not None:
+        _check_shape(t, shape, name)
     return t
+
+
+def _check_shape(t, shape, name):
+    if t.dim() != len(shape) or any(want is not None and got != want
+                                    for got, want in zip(t.shape, shape)):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected "
+                         f"{tuple('*' if w is None else w for w in shape)}")
+
+
+def _opt(t, dtype, name, shape):
+    return None if t is None else _dev(t, dtype, name, shape)
+
+
+def _out(out, like, name="out"):
+    if out is None:
+        return torch.empty_like(like)
+    return _dev(out, like.dtype, name, tuple(like.shape))
 
 
 def check_device() -> int:
@@ -238,13 +260,21 @@ def new_status(device="cuda"):
 
 # ------------------------------------------------------------------ the hot path
 
+def _rope_args(q, k, v, positions, slot_mapping, table, status):
+    _dev(q, torch.float16, "q", (None, None, None))
+    T, H, d = q.shape
+    _dev(k, torch.float16, "k", (T, None, d))
+    _dev(v, torch.float16, "v", tuple(k.shape))
+    _dev(positions, torch.int32, "positions", (T,))
+    _dev(slot_mapping, torch.int32, "slot_mapping", (T,))
+    _dev(table, torch.float32, "table", (None, d // 2, 2))
+    _opt(status, torch.int32, "status", (1,))
+    return T, H, k.shape[1], d
+
+
 def rope_kv_write(q, k, v, positions, slot_mapping, table, cache: Cache, layer=0, status=None,
                   stream=None):
-    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
-    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
-    _dev(table, torch.float32, "table")
-    T, H, d = q.shape
-    Hk = k.shape[1]
+    T, H, Hk, d = _rope_args(q, k, v, positions, slot_mapping, table, status)
     _check("pa_rope_kv_write", lib().pa_rope_kv_write(
         _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), T, H, Hk, d, _p(table),
         table.shape[0], ctypes.byref(cache.desc), layer, _p(status), _stream(stream)))
@@ -252,14 +282,17 @@ def rope_kv_write(q, k, v, positions, slot_mapping, table, cache: Cache, layer=0
 
 def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_seqlen_q,
                    n_kv_heads, layer=0, scale=0.0, out=None, status=None, stream=None):
-    _dev(q, torch.float16, "q"); _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q")
-    _dev(cu_seqlens_k, torch.int32, "cu_seqlens_k"); _dev(block_tables, torch.int32, "block_tables")
+    _dev(q, torch.float16, "q", (None, None, None))
     T, H, d = q.shape
-    if out is None:
-        out = torch.empty_like(q)
+    _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q", (None,))
+    B = cu_seqlens_q.shape[0] - 1
+    _dev(cu_seqlens_k, torch.int32, "cu_seqlens_k", (B + 1,))
+    _dev(block_tables, torch.int32, "block_tables", (B, None))
+    _opt(status, torch.int32, "status", (1,))
+    out = _out(out, q)
     _check("pa_prefill_varlen", lib().pa_prefill_varlen(
         _p(q), T, ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
-        _p(block_tables), block_tables.shape[1], cu_seqlens_q.shape[0] - 1, int(max_seqlen_q), H,
+        _p(block_tables), block_tables.shape[1], B, int(max_seqlen_q), H,
         n_kv_heads, d, float(scale), _p(out), _p(status), _stream(stream)))
     return out
 
@@ -275,13 +308,20 @@ def decode_workspace(num_seqs, n_heads, n_kv_heads, head_dim, device="cuda", nby
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
+def _decode_args(q, block_tables, context_lens, workspace, status):
+    _dev(q, torch.float16, "q", (None, None, None))
+    B = q.shape[0]
+    _dev(block_tables, torch.int32, "block_tables", (B, None))
+    _dev(context_lens, torch.int32, "context_lens", (B,))
+    _dev(workspace, torch.uint8, "workspace", (None,))
+    _opt(status, torch.int32, "status", (1,))
+    return q.shape
+
+
 def decode(q, cache: Cache, block_tables, context_lens, workspace, n_kv_heads, layer=0, scale=0.0,
            out=None, status=None, stream=None):
-    _dev(q, torch.float16, "q"); _dev(block_tables, torch.int32, "block_tables")
-    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
-    B, H, d = q.shape
-    if out is None:
-        out = torch.empty_like(q)
+    B, H, d = _decode_args(q, block_tables, context_lens, workspace, status)
+    out = _out(out, q)
     _check("pa_decode", lib().pa_decode(
         _p(q), ctypes.byref(cache.desc), layer, _p(block_tables), block_tables.shape[1],
         _p(context_lens), B, H, n_kv_heads, d, float(scale), _p(workspace), workspace.numel(),
@@ -291,11 +331,9 @@ def decode(q, cache: Cache, block_tables, context_lens, workspace, n_kv_heads, l
 
 def _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables, context_lens,
                workspace, n_kv_heads, layer, scale, out, status):
-    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
-    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
-    _dev(rope_table, torch.float32, "rope_table"); _dev(block_tables, torch.int32, "block_tables")
-    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
-    B, H, d = q.shape
+    _rope_args(q, k, v, positions, slot_mapping, rope_table, status)
+    B, H, d = _decode_args(q, block_tables, context_lens, workspace, status)
+    _dev(out, torch.float16, "out", (B, H, d))
     return [_p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), _p(rope_table),
             rope_table.shape[0], ctypes.byref(cache.desc), layer, _p(block_tables),
             block_tables.shape[1], _p(context_lens), B, H, n_kv_heads, d, float(scale),
@@ -306,8 +344,7 @@ def decode_step(q, k, v, positions, slot_mapping, rope_table, cache: Cache, bloc
                 context_lens, workspace, n_kv_heads, layer=0, scale=0.0, out=None, status=None,
                 stream=None):
     """pa_decode_step: RoPE + append of the new tokens, then decode."""
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out(out, q)
     args = _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
                       context_lens, workspace, n_kv_heads, layer, scale, out, status)
     _check("pa_decode_step", lib().pa_decode_step(*args, _stream(stream)))
@@ -323,7 +360,7 @@ class StepGraph:
     def __init__(self, q, k, v, positions, slot_mapping, rope_table, cache: Cache, block_tables,
                  context_lens, workspace, n_kv_heads, layer=0, scale=0.0, out=None,
                  status=None):
-        self.out = torch.empty_like(q) if out is None else out
+        self.out = _out(out, q)
         self._keep = (q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
                       context_lens, workspace, status)
         args = _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
@@ -421,7 +458,7 @@ class BlockManager:
 
 def selftest_wait_timeout(status, stream=None):
     """pa_selftest_wait_timeout: a bounded wait that runs out (about 1 s)."""
-    _dev(status, torch.int32, "status")
+    _dev(status, torch.int32, "status", (1,))
     _check("pa_selftest_wait_timeout", lib().pa_selftest_wait_timeout(_p(status), _stream(stream)))
 
 
@@ -450,22 +487,16 @@ class CacheI8:
 
 def rope_kv_write_i8(q, k, v, positions, slot_mapping, table, cache: CacheI8, layer=0,
                      status=None, stream=None):
-    _dev(q, torch.float16, "q"); _dev(k, torch.float16, "k"); _dev(v, torch.float16, "v")
-    _dev(positions, torch.int32, "positions"); _dev(slot_mapping, torch.int32, "slot_mapping")
-    _dev(table, torch.float32, "table")
-    T, H, d = q.shape
+    T, H, Hk, d = _rope_args(q, k, v, positions, slot_mapping, table, status)
     _check("pa_rope_kv_write_i8", lib().pa_rope_kv_write_i8(
-        _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), T, H, k.shape[1], d, _p(table),
+        _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), T, H, Hk, d, _p(table),
         table.shape[0], ctypes.byref(cache.desc), layer, _p(status), _stream(stream)))
 
 
 def decode_i8(q, cache: CacheI8, block_tables, context_lens, workspace, n_kv_heads, layer=0,
               scale=0.0, out=None, status=None, stream=None):
-    _dev(q, torch.float16, "q"); _dev(block_tables, torch.int32, "block_tables")
-    _dev(context_lens, torch.int32, "context_lens"); _dev(workspace, torch.uint8, "workspace")
-    B, H, d = q.shape
-    if out is None:
-        out = torch.empty_like(q)
+    B, H, d = _decode_args(q, block_tables, context_lens, workspace, status)
+    out = _out(out, q)
     _check("pa_decode_i8", lib().pa_decode_i8(
         _p(q), ctypes.byref(cache.desc), layer, _p(block_tables), block_tables.shape[1],
         _p(context_lens), B, H, n_kv_heads, d, float(scale), _p(workspace), workspace.numel(),

@@ -164,3 +164,16 @@ def test_prepare_prefill_no_sequences_accepts_null_outputs(libpa):
     md = pa.prepare_prefill([], [], np.zeros((0, 1), np.int32))
     assert md["cu_seqlens_q"].tolist() == [0] and md["cu_seqlens_k"].tolist() == [0]
     assert md["max_seqlen_q"] == 0 and md["max_seqlen_k"] == 0
+
+
+def test_binding_shape_rule():
+    """The binding's size check (the library sees only pointers): exact
+    extents, None entries free, rank must match."""
+    import torch
+    t = torch.empty(4, 2, 64)
+    pa._check_shape(t, (4, None, 64), "x")
+    for bad in ((3, None, 64), (4, 2), (4, 2, 64, 1), (None, 3, None)):
+        with pytest.raises(ValueError):
+            pa._check_shape(t, bad, "x")
+    with pytest.raises(TypeError):
+        pa._dev(t.half(), torch.float16, "x", (4, 2, 64))  # a host tensor

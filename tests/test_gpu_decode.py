@@ -232,3 +232,29 @@ def test_rope_bad_position_and_slot():
                      torch.tensor([-1], dtype=torch.int32, device="cuda"), table, cache, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+
+
+def test_binding_rejects_mismatched_buffers_before_launch():
+    """Buffers whose sizes disagree with q are refused on the host (the
+    kernels would index past them): nothing is launched."""
+    case, init = custom_case(4, 2, 64, [5, 40], seed=12)
+    run = DecodeRun(case, init)
+    T, Hk, d = run.k.shape
+    with pytest.raises(ValueError):
+        pa.rope_kv_write(run.q, run.k, run.v[:T - 1].contiguous(), run.positions, run.slots,
+                         run.table, run.cache)
+    with pytest.raises(ValueError):
+        pa.rope_kv_write(run.q, run.k, run.v, run.positions[:T - 1], run.slots, run.table,
+                         run.cache)
+    with pytest.raises(ValueError):
+        pa.decode(run.q, run.cache, run.bt, run.ctx[:1], run.ws, Hk)
+    with pytest.raises(ValueError):
+        pa.decode(run.q, run.cache, run.bt, run.ctx, run.ws, Hk,
+                  out=torch.empty(1, 1, d, dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        pa.decode(run.q, run.cache, run.bt, run.ctx, run.ws, Hk,
+                  status=torch.zeros(2, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(run.status.item()) == 0
+    out = run.run()  # the same buffers, well formed, still go through
+    assert_attention_close(out, oracle_decode_step(case, init)[3])
