@@ -168,6 +168,24 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 // int8: four CTAs per SM (96 registers; the Q fragments live in shared
 // memory): the per-block consumer work, not the bytes in flight, bounds the
 // int8 pipeline, so more consumer warps pay.
+// Online-softmax merge factors of n partial results of head h, given as
+// (max, sum) in column h of the rows of m and l (row stride kGroupPad):
+// M = max_i m_i; f_i = 2^(m_i - M) replaces m_i (all zero when every m_i is
+// -inf, an empty part); L = sum_i f_i l_i goes to l[h] and M to
+// l[kGroupPad + h].  O = sum_i f_i O_i is then the merged numerator.
+__device__ __forceinline__ void merge_factors(float *m, float *l, int h, int n) {
+    float M = -INFINITY;
+    for (int i = 0; i < n; ++i) M = fmaxf(M, m[i * kGroupPad + h]);
+    float Lsum = 0.f;
+    for (int i = 0; i < n; ++i) {
+        const float f = M == -INFINITY ? 0.f : ex2(m[i * kGroupPad + h] - M);
+        m[i * kGroupPad + h] = f;
+        Lsum += f * l[i * kGroupPad + h];
+    }
+    l[h] = Lsum;
+    l[kGroupPad + h] = M;
+}
+
 template <int D, int NSTAGE, bool I8>
 __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap,
@@ -610,24 +628,19 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
         }
         named_barrier_sync(1, kCons);
         abort = sm_flag[1] != 0;
+        if (tid < a.g) merge_factors(sm_m, sm_l, tid, kConsumerWarps);
+        named_barrier_sync(1, kCons);
 
         const bool whole = pos == sg.pair_start && pos + nb == sg.pair_end;
         const int slot = pos == start ? 0 : 1;
         float *myrec = a.rec + ((int64_t)(cta * 2 + slot) * kGroupPad) * L::kRec;
         for (int idx = tid; idx < a.g * D; idx += kCons) {
             const int h = idx / D, d = idx - (idx / D) * D;
-            float M = -INFINITY;
+            float O = 0.f;
 #pragma unroll
-            for (int wv = 0; wv < kConsumerWarps; ++wv) M = fmaxf(M, sm_m[wv * kGroupPad + h]);
-            float O = 0.f, Lsum = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int wv = 0; wv < kConsumerWarps; ++wv) {
-                    const float f = ex2(sm_m[wv * kGroupPad + h] - M);
-                    Lsum += f * sm_l[wv * kGroupPad + h];
-                    O += f * sm_o[(wv * kGroupPad + h) * D + d];
-                }
-            }
+            for (int wv = 0; wv < kConsumerWarps; ++wv)
+                O += sm_m[wv * kGroupPad + h] * sm_o[(wv * kGroupPad + h) * D + d];
+            const float Lsum = sm_l[h];
             if (whole) {
                 a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
                     __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
@@ -635,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
                 float *r = myrec + h * L::kRec;
                 r[d] = O;
                 if (d == 0) {
-                    r[D] = M;
+                    r[D] = sm_l[kGroupPad + h];
                     r[D + 1] = Lsum;
                 }
             }
@@ -652,62 +665,61 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
             named_barrier_sync(1, kCons);
             const int nrec = c_last - c_first + 1;  // pieces of the pair
             if (sm_flag[0] && nrec <= kConsumerWarps) {
-                // Merge of up to 4 pieces.  The pieces' (max, sum) per head go
-                // through shared memory (the [4][8] areas are free now), then
-                // each thread reads the O values of four of its (head, column)
-                // elements of one piece with independent loads, piece after
-                // piece, so the merge costs a few L2 round trips, not one
-                // per element.
+                // Merge of up to 4 pieces.  Each thread loads the O values of
+                // its (head, column) elements of every piece together, beside
+                // the pieces' (max, sum) per head, so the merge costs one or
+                // two L2 round trips; the factors per (piece, head) are
+                // computed once, in shared memory (the [4][8] areas are free).
                 __threadfence();
-                auto piece = [&](int i, int h) {
-                    const int c = c_first + i;
+                const float *pb[kConsumerWarps];
+#pragma unroll
+                for (int i = 0; i < kConsumerWarps; ++i) {
+                    const int c = c_first + (i < nrec ? i : 0);
                     const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                    return a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
-                };
+                    pb[i] = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
+                }
+                // Elements tid + k * kCons; the int8 kernel (register count
+                // capped for four CTAs per SM) loads them all in one pass, the
+                // fp16 one in passes of four (two CTAs per SM need <= 168
+                // registers a thread).
+                constexpr int kEl = kGroupPad * D / kCons;
+                constexpr int kPass = I8 || kEl < 4 ? kEl : 4;
                 if (tid < nrec * a.g) {
                     const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
-                    const float *r = piece(i, h);
+                    const float *r = pb[i] + h * L::kRec;
                     sm_m[i * kGroupPad + h] = __ldcg(r + D);
                     sm_l[i * kGroupPad + h] = __ldcg(r + D + 1);
                 }
-                named_barrier_sync(1, kCons);
-                // Elements tid + k * 128 (k < 8 at most), four at a time.
-                constexpr int kEl = 4;
 #pragma unroll 1
-                for (int k0 = 0; k0 < kGroupPad * D / kCons; k0 += kEl) {
-                    float Mv[kEl], Lv[kEl], Ov[kEl];
+                for (int k0 = 0; k0 < kEl; k0 += kPass) {
+                    float x[kConsumerWarps][kPass];
 #pragma unroll
-                    for (int k = 0; k < kEl; ++k) {
-                        const int idx = tid + (k0 + k) * kCons, h = idx / D;
-                        Mv[k] = -INFINITY;
-                        Lv[k] = Ov[k] = 0.f;
-                        if (idx < a.g * D)
-                            for (int i = 0; i < nrec; ++i)
-                                Mv[k] = fmaxf(Mv[k], sm_m[i * kGroupPad + h]);
-                    }
-                    for (int i = 0; i < nrec; ++i) {
-                        float x[kEl];
+                    for (int i = 0; i < kConsumerWarps; ++i) {
 #pragma unroll
-                        for (int k = 0; k < kEl; ++k) {
+                        for (int k = 0; k < kPass; ++k) {
                             const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
-                            x[k] = idx < a.g * D ? __ldcg(piece(i, h) + d) : 0.f;
-                        }
-#pragma unroll
-                        for (int k = 0; k < kEl; ++k) {
-                            const int idx = tid + (k0 + k) * kCons, h = idx / D;
-                            if (idx < a.g * D && Mv[k] != -INFINITY) {
-                                const float f = ex2(sm_m[i * kGroupPad + h] - Mv[k]);
-                                Lv[k] += f * sm_l[i * kGroupPad + h];
-                                Ov[k] += f * x[k];
-                            }
+                            x[i][k] = i < nrec && idx < a.g * D
+                                          ? __ldcg(pb[i] + h * L::kRec + d)
+                                          : 0.f;
                         }
                     }
+                    if (k0 == 0) {
+                        named_barrier_sync(1, kCons);
+                        if (tid < a.g) merge_factors(sm_m, sm_l, tid, nrec);
+                        named_barrier_sync(1, kCons);
+                    }
 #pragma unroll
-                    for (int k = 0; k < kEl; ++k) {
+                    for (int k = 0; k < kPass; ++k) {
                         const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
-                        if (idx < a.g * D)
+                        if (idx < a.g * D) {
+                            float O = 0.f;
+#pragma unroll
+                            for (int i = 0; i < kConsumerWarps; ++i)
+                                if (i < nrec) O += sm_m[i * kGroupPad + h] * x[i][k];
+                            const float Lsum = sm_l[h];
                             a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
-                                __float2half_rn(Lv[k] > 0.f ? Ov[k] / Lv[k] : 0.f);
+                                __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
+                        }
                     }
                 }
                 if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
