@@ -108,6 +108,26 @@ def test_int8_decode_edge_lengths(H, Hk, d):
     check(case, codes, scales)
 
 
+@pytest.mark.parametrize("ctxs,Hk,ctas,g,d", [([5000], 1, 2, 8, 128), ([5000], 1, 4, 8, 128),
+                                              ([5000], 1, 5, 8, 128), ([2000, 3000], 2, 3, 4, 64),
+                                              ([4100, 100], 8, 3, 8, 128)])
+def test_int8_narrow_grid_merges_pieces(ctxs, Hk, ctas, g, d):
+    """The int8 kernel's merges (a pair cut into 2, 4 or 5 pieces by a
+    workspace with record slots for only a few CTAs) give the same result as
+    the decode formula on code * scale."""
+    H = g * Hk
+    case, init = custom_case(H, Hk, d, ctxs, seed=900 + sum(ctxs) + ctas)
+    codes, scales = quantize_cache(init)
+    run = I8Run(case, codes, scales)
+    slot_bytes = 2 * 8 * (d + 4) * 4
+    counters = (len(ctxs) * Hk * 4 + 255) // 256 * 256
+    run.ws = pa.decode_workspace(len(ctxs), H, Hk, d, nbytes=counters + ctas * slot_bytes)
+    out = run.run()
+    *_, want = oracle_step(case, codes, scales)
+    assert int(run.status.item()) == 0
+    assert_attention_close(out, want)
+
+
 def test_int8_ignores_garbage_in_unwritten_slots():
     """Codes and scales past a sequence's context may hold anything (NaN
     scales included): the output must not see them."""
