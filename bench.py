@@ -23,8 +23,9 @@ steps.  Per-kernel durations of the dominant kernel come from events around
 its launches inside the same timed loop.  `e2e` repeats the step through the
 library's calls with the step's inputs copied from pinned host memory (one
 copy of a buffer that holds them all) and the output copied back inside the
-timed region; for fp16 decode the step runs as the captured step graph
-(pa_step_graph_launch), as a serving loop would replay it.
+timed region; for fp16 decode the step runs as the captured step graph with
+both copies inside it (pa_step_graph_create_io), as a serving loop would
+replay it: one launch per step.
 
     --int8   decode workloads: the int8 KV cache path (pa_rope_kv_write_i8 +
              pa_decode_i8) as the timed step.
@@ -222,9 +223,10 @@ class DecodeBench:
             ev[1].record()
 
     def e2e_setup(self):
-        """Inputs from pinned host memory (one copy), the step (replayed as
-        the captured step graph where there is one), output back to pinned
-        host memory."""
+        """Inputs from pinned host memory (one copy), the step, output back
+        to pinned host memory.  Where there is a captured step graph, both
+        copies are inside it (pa_step_graph_create_io): one replay per
+        step."""
         torch = self.torch
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.e2e_graph = None
@@ -232,15 +234,17 @@ class DecodeBench:
             pa, d, wl = self.pa, self.d, self.case.wl
             self.e2e_graph = pa.StepGraph(d["q"], d["k"], d["v"], d["positions"], d["slots"],
                                           self.table, self.cache, d["bt"], d["ctx"], self.ws,
-                                          wl.n_kv_heads, out=self.out, status=self.status)
+                                          wl.n_kv_heads, out=self.out, status=self.status,
+                                          host_in=self.packed.host, dev_in=self.packed.device,
+                                          host_out=self.out_host)
         return self.packed.nbytes, self.out_host.numel() * self.out_host.element_size()
 
     def e2e_step(self):
-        self.packed.upload()
         if self.e2e_graph is not None:
             self.e2e_graph.launch()
-        else:
-            self.step()
+            return
+        self.packed.upload()
+        self.step()
         self.out_host.copy_(self.out, non_blocking=True)
 
     def e2e_close(self):

@@ -313,6 +313,33 @@ int pa_step_graph_launch(pa_step_graph_t graph, pa_stream_t stream);
 int pa_step_graph_destroy(pa_step_graph_t graph);
 
 /*
+ * The same captured step with its host I/O inside the graph, so that one
+ * replay moves a step's inputs in, runs it and brings its result back:
+ *   first   in_bytes from host_in to dev_in (host to device), where dev_in
+ *           is the device buffer that holds the step's inputs (q, k, v,
+ *           positions, slot_mapping, block_tables, context_lens or any of
+ *           them, laid out by the caller);
+ *   then    pa_decode_step with the other arguments, as pa_step_graph_create;
+ *   last    the output, num_seqs * n_heads * head_dim fp16, from `out` to
+ *           host_out (device to host).
+ * host_in and host_out must be page-locked host memory (cudaHostAlloc,
+ * cudaMallocHost or registered) that stays alive until the graph is
+ * destroyed; the caller fills host_in before a replay and reads host_out
+ * after it has completed (e.g. after synchronising the replay's stream).
+ * in_bytes = 0 leaves out the input copy, host_out = NULL the output copy.
+ * Errors: those of pa_step_graph_create, and PA_ERR_INVALID for a missing
+ * or pageable host buffer (nothing is created).
+ */
+int pa_step_graph_create_io(pa_step_graph_t *graph, void *q, void *k, const void *v,
+                            const int32_t *positions, const int32_t *slot_mapping,
+                            const void *rope_table, int max_positions, const pa_cache_t *cache,
+                            int layer, const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs, int n_heads,
+                            int n_kv_heads, int head_dim, float scale, void *workspace,
+                            size_t workspace_bytes, void *out, int32_t *dev_status,
+                            const void *host_in, void *dev_in, size_t in_bytes, void *host_out);
+
+/*
  * Self-test of the kernels' failure detection; the pages have no
  * counterpart.  Every wait inside a libpa kernel (an mbarrier phase) is
  * bounded: after about a second it gives up, ORs PA_DEV_TIMEOUT into the

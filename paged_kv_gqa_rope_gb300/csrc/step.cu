@@ -29,16 +29,35 @@ extern "C" int pa_decode_step(void *q, void *k, const void *v, const int32_t *po
                      dev_status, stream);
 }
 
-extern "C" int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, const void *v,
-                                    const int32_t *positions, const int32_t *slot_mapping,
-                                    const void *rope_table, int max_positions,
-                                    const pa_cache_t *cache, int layer,
-                                    const int32_t *block_tables, int max_blocks_per_seq,
-                                    const int32_t *context_lens, int num_seqs, int n_heads,
-                                    int n_kv_heads, int head_dim, float scale, void *workspace,
-                                    size_t workspace_bytes, void *out, int32_t *dev_status) {
+namespace {
+
+// True if p is host memory the device can copy from asynchronously
+// (page-locked: allocated by cudaHostAlloc / cudaMallocHost or registered).
+bool page_locked(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
+extern "C" int pa_step_graph_create_io(
+    pa_step_graph_t *graph, void *q, void *k, const void *v, const int32_t *positions,
+    const int32_t *slot_mapping, const void *rope_table, int max_positions,
+    const pa_cache_t *cache, int layer, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+    float scale, void *workspace, size_t workspace_bytes, void *out, int32_t *dev_status,
+    const void *host_in, void *dev_in, size_t in_bytes, void *host_out) {
     if (!graph) return PA_ERR_INVALID;
     *graph = nullptr;
+    if (in_bytes > 0 && (!host_in || !dev_in)) return PA_ERR_INVALID;
+    if (in_bytes > 0 && !page_locked(host_in)) return PA_ERR_INVALID;
+    if (host_out && (!out || num_seqs <= 0 || !page_locked(host_out))) return PA_ERR_INVALID;
+    const size_t out_bytes =
+        host_out ? (size_t)num_seqs * (size_t)n_heads * (size_t)head_dim * 2 : 0;
     cudaStream_t cs = nullptr;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
         cudaGetLastError();
@@ -50,10 +69,17 @@ extern "C" int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, co
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
         rc = PA_ERR_CUDA;
     } else {
-        rc = pa_decode_step(q, k, v, positions, slot_mapping, rope_table, max_positions, cache,
-                            layer, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                            n_heads, n_kv_heads, head_dim, scale, workspace, workspace_bytes,
-                            out, dev_status, cs);
+        if (in_bytes > 0 &&
+            cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            rc = PA_ERR_CUDA;
+        if (rc == PA_OK)
+            rc = pa_decode_step(q, k, v, positions, slot_mapping, rope_table, max_positions,
+                                cache, layer, block_tables, max_blocks_per_seq, context_lens,
+                                num_seqs, n_heads, n_kv_heads, head_dim, scale, workspace,
+                                workspace_bytes, out, dev_status, cs);
+        if (rc == PA_OK && out_bytes > 0 &&
+            cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+            rc = PA_ERR_CUDA;
         // End the capture whatever happened, so the stream is usable again.
         if (cudaStreamEndCapture(cs, &g) != cudaSuccess && rc == PA_OK) rc = PA_ERR_CUDA;
     }
@@ -73,6 +99,21 @@ extern "C" int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, co
     h->exec = exec;
     *graph = h;
     return PA_OK;
+}
+
+extern "C" int pa_step_graph_create(pa_step_graph_t *graph, void *q, void *k, const void *v,
+                                    const int32_t *positions, const int32_t *slot_mapping,
+                                    const void *rope_table, int max_positions,
+                                    const pa_cache_t *cache, int layer,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, int num_seqs, int n_heads,
+                                    int n_kv_heads, int head_dim, float scale, void *workspace,
+                                    size_t workspace_bytes, void *out, int32_t *dev_status) {
+    return pa_step_graph_create_io(graph, q, k, v, positions, slot_mapping, rope_table,
+                                   max_positions, cache, layer, block_tables, max_blocks_per_seq,
+                                   context_lens, num_seqs, n_heads, n_kv_heads, head_dim, scale,
+                                   workspace, workspace_bytes, out, dev_status, nullptr, nullptr,
+                                   0, nullptr);
 }
 
 extern "C" int pa_step_graph_launch(pa_step_graph_t graph, pa_stream_t stream) {

@@ -25,7 +25,7 @@ EXPORTS = (
     "pa_prepare_decode", "pa_rope_table_bytes", "pa_rope_table_init", "pa_rope_kv_write",
     "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
     "pa_check_device", "pa_decode_noalloc", "pa_decode_step", "pa_step_graph_create",
-    "pa_step_graph_launch", "pa_step_graph_destroy",
+    "pa_step_graph_launch", "pa_step_graph_destroy", "pa_step_graph_create_io",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_blocks_needed", "pa_bm_allocate",
     "pa_bm_next_chunk", "pa_bm_mark_computed", "pa_bm_can_append", "pa_bm_append",
     "pa_bm_num_tokens", "pa_bm_block_table", "pa_bm_free", "pa_selftest_wait_timeout",
@@ -81,6 +81,10 @@ _SIGS = {
     "pa_step_graph_create": (_i32, [ctypes.POINTER(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                     ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
                                     _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp]),
+    "pa_step_graph_create_io": (_i32, [ctypes.POINTER(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                       ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
+                                       _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp, _vp, _vp,
+                                       _sz, _vp]),
     "pa_step_graph_launch": (_i32, [_vp, _vp]),
     "pa_step_graph_destroy": (_i32, [_vp]),
     "pa_bm_create": (_vp, [_i32, _i32]),
@@ -355,18 +359,42 @@ class StepGraph:
     """pa_step_graph_*: a decode step captured once, replayed by launch().
     The tensors passed in are the step's buffers for every replay; refill
     them in place between replays.  References are kept so they outlive
-    the graph."""
+    the graph.
+
+    With `host_in` (a pinned uint8 host tensor) and `dev_in` (the device
+    uint8 tensor of the same size that the input tensors are views of), a
+    replay first copies host_in to dev_in; with `host_out` (a pinned host
+    tensor shaped like q), it ends by copying the output there
+    (pa_step_graph_create_io): one launch per step, I/O included."""
 
     def __init__(self, q, k, v, positions, slot_mapping, rope_table, cache: Cache, block_tables,
                  context_lens, workspace, n_kv_heads, layer=0, scale=0.0, out=None,
-                 status=None):
+                 status=None, host_in=None, dev_in=None, host_out=None):
         self.out = _out(out, q)
         self._keep = (q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
-                      context_lens, workspace, status)
+                      context_lens, workspace, status, host_in, dev_in, host_out)
         args = _step_args(q, k, v, positions, slot_mapping, rope_table, cache, block_tables,
                           context_lens, workspace, n_kv_heads, layer, scale, self.out, status)
         h = ctypes.c_void_p()
-        _check("pa_step_graph_create", lib().pa_step_graph_create(ctypes.byref(h), *args))
+        if host_in is None and dev_in is None and host_out is None:
+            _check("pa_step_graph_create", lib().pa_step_graph_create(ctypes.byref(h), *args))
+        else:
+            nin = 0
+            if host_in is not None or dev_in is not None:
+                if not (isinstance(host_in, torch.Tensor) and not host_in.is_cuda
+                        and host_in.is_pinned() and host_in.dtype == torch.uint8
+                        and host_in.is_contiguous()):
+                    raise TypeError("host_in must be a contiguous pinned host uint8 tensor")
+                _dev(dev_in, torch.uint8, "dev_in", (host_in.numel(),))
+                nin = host_in.numel()
+            if host_out is not None:
+                if not (isinstance(host_out, torch.Tensor) and not host_out.is_cuda
+                        and host_out.is_pinned() and host_out.dtype == torch.float16
+                        and host_out.is_contiguous()):
+                    raise TypeError("host_out must be a contiguous pinned host fp16 tensor")
+                _check_shape(host_out, tuple(q.shape), "host_out")
+            _check("pa_step_graph_create_io", lib().pa_step_graph_create_io(
+                ctypes.byref(h), *args, _p(host_in), _p(dev_in), nin, _p(host_out)))
         self._h = h
 
     def launch(self, stream=None):

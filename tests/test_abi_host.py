@@ -119,6 +119,14 @@ def test_kernel_entry_points_validate_before_launch(libpa):
 
 
 def test_step_graph_rejects_null_handles(libpa):
+    assert libpa.pa_step_graph_create_io(None, *([None] * 6), 0, None, 0, None, 0, None, 1, 8, 8,
+                                         128, 0.0, None, 0, None, None, None, None, 0,
+                                         None) == pa.PA_ERR_INVALID
+    h = ctypes.c_void_p()
+    # an input copy needs both buffers
+    assert libpa.pa_step_graph_create_io(ctypes.byref(h), *([None] * 6), 0, None, 0, None, 0,
+                                         None, 1, 8, 8, 128, 0.0, None, 0, None, None, None,
+                                         None, 64, None) == pa.PA_ERR_INVALID
     assert libpa.pa_step_graph_launch(None, None) == pa.PA_ERR_INVALID
     assert libpa.pa_step_graph_destroy(None) == pa.PA_ERR_INVALID
     assert libpa.pa_step_graph_create(None, *([None] * 6), 0, None, 0, None, 0, None,

@@ -100,3 +100,80 @@ def test_step_graph_launches_on_any_stream():
     s.synchronize()
     g.close()
     assert torch.equal(out, want)
+
+
+def _packed(arrays):
+    """Host arrays laid out in one pinned uint8 buffer (256-byte aligned
+    offsets) and device views of a device buffer of the same layout."""
+    off, lay = 0, {}
+    for k, a in arrays.items():
+        lay[k] = (off, a)
+        off = (off + a.nbytes + 255) // 256 * 256
+    host = torch.zeros(off, dtype=torch.uint8).pin_memory()
+    dev = torch.zeros(off, dtype=torch.uint8, device="cuda")
+    views = {k: dev[o:o + a.nbytes].view(torch.from_numpy(a).dtype).view(a.shape)
+             for k, (o, a) in lay.items()}
+
+    def fill(new):
+        hv = host.numpy()
+        for k, a in new.items():
+            o, ref = lay[k]
+            a = np.ascontiguousarray(a, ref.dtype)
+            hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+    return host, dev, views, fill
+
+
+def test_step_graph_with_host_io_replays_a_serving_loop():
+    """pa_step_graph_create_io: each replay copies the step's inputs from
+    pinned host memory, runs RoPE/append + decode and copies the output
+    back; the device input buffers are never written any other way."""
+    ctxs = [5, 100, 1000, 2999]
+    case, init = custom_case(16, 4, 128, ctxs, seed=25)
+    run = DecodeRun(case, init, table_rows=4096)
+    md = orc.decode_metadata(case.num_cached, case.block_tables, 16)
+    step_in = lambda c, m: dict(q=c.q, k=c.k, v=c.v,  # noqa: E731
+                                positions=m["positions"].astype(np.int32),
+                                slots=m["slot_mapping"].astype(np.int32),
+                                ctx=m["context_lens"].astype(np.int32),
+                                bt=c.block_tables.astype(np.int32))
+    host, dev, d, fill = _packed(step_in(case, md))
+    host_out = torch.zeros(tuple(run.q.shape), dtype=torch.float16).pin_memory()
+    g = pa.StepGraph(d["q"], d["k"], d["v"], d["positions"], d["slots"], run.table, run.cache,
+                     d["bt"], d["ctx"], run.ws, case.wl.n_kv_heads, status=run.status,
+                     host_in=host, dev_in=dev, host_out=host_out)
+    rng = np.random.default_rng(26)
+    cache_np = init
+    try:
+        for step in range(3):
+            fill(step_in(case, md))
+            g.launch()
+            torch.cuda.synchronize()
+            assert int(run.status.item()) == 0
+            q_rot, _, cache_np, want = oracle_decode_step(case, cache_np)
+            assert np.array_equal(bits(d["q"]), bits(q_rot)), f"step {step}: rotated Q"
+            assert torch.equal(run.cache.tensor, torch.from_numpy(cache_np).cuda()), \
+                f"step {step}: cache"
+            assert torch.equal(host_out, g.out.cpu()), f"step {step}: output copied back"
+            assert_attention_close(host_out.cuda(), want)
+            case = next_step(case, rng)
+            md = orc.decode_metadata(case.num_cached, case.block_tables, 16)
+    finally:
+        g.close()
+
+
+def test_step_graph_io_refuses_pageable_host_memory(libpa):
+    import ctypes
+    case, init = custom_case(8, 8, 64, [17, 300], seed=27)
+    b = DecodeRun(case, init)
+    args = pa._step_args(b.q, b.k, b.v, b.positions, b.slots, b.table, b.cache, b.bt, b.ctx,
+                         b.ws, case.wl.n_kv_heads, 0, 0.0, torch.empty_like(b.q), b.status)
+    pageable = np.zeros(1024, np.uint8)
+    dev = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    h = ctypes.c_void_p()
+    rc = libpa.pa_step_graph_create_io(ctypes.byref(h), *args, pa._p(pageable), pa._p(dev), 1024,
+                                       None)
+    assert rc == pa.PA_ERR_INVALID and not h.value
+    out_pageable = np.zeros(tuple(b.q.shape), np.float16)
+    rc = libpa.pa_step_graph_create_io(ctypes.byref(h), *args, None, None, 0,
+                                       pa._p(out_pageable))
+    assert rc == pa.PA_ERR_INVALID and not h.value
