@@ -185,3 +185,51 @@ def test_binding_shape_rule():
             pa._check_shape(t, bad, "x")
     with pytest.raises(TypeError):
         pa._dev(t.half(), torch.float16, "x", (4, 2, 64))  # a host tensor
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "pa.h"
+#include "pa_block_manager.h"
+
+int main(void) {
+    /* two sequences: 5 and 17 tokens cached, blocks {3} and {7, 2} */
+    const int32_t cached[2] = {5, 17};
+    const int32_t tables[4] = {3, -1, 7, 2};
+    int32_t pos[2], slot[2], ctx[2];
+    int rc = pa_prepare_decode(2, cached, tables, 2, 16, pos, slot, ctx);
+    pa_bm_t bm = pa_bm_create(4, 16);
+    int32_t toks[20];
+    int i, hit = -1;
+    for (i = 0; i < 20; ++i) toks[i] = i;
+    if (bm) pa_bm_allocate(bm, 1, toks, 20, &hit);
+    printf("%d %d %d %d %d %d %d %lu %d %s\n", rc, pos[0], slot[0], ctx[0], pos[1], slot[1],
+           ctx[1], (unsigned long)pa_cache_bytes(1, 4, 16, 2, 64),
+           bm ? pa_bm_num_free(bm) : -1, pa_strerror(PA_ERR_WORKSPACE));
+    pa_bm_destroy(bm);
+    return 0;
+}
+"""
+
+
+def test_c_client_links_and_calls_the_library(libpa, tmp_path):
+    """The boundary is plain C: a C99 program that includes the headers,
+    links libpa.so and calls host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    libdir = os.path.dirname(pa.LIB_PATH)
+    exe = tmp_path / "client"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", INCLUDE,
+                    str(src), "-o", str(exe), "-L", libdir, "-lpa", "-Wl,-rpath," + libdir],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    # position 5 -> block 3 slot 53; position 17 -> logical block 1 = 2, slot 33
+    assert out[:7] == ["0", "5", "53", "6", "17", "33", "18"]
+    assert int(out[7]) == 2 * 4 * 16 * 2 * 64 * 2
+    assert out[8] == "2"  # 20 tokens took two of the four blocks
+    assert " ".join(out[9:]) == "decode workspace too small"
