@@ -14,7 +14,8 @@ The headline workload is the Llama-2-7B-shaped MHA decode (32 heads, d=128,
 batch 32, 2048 cached tokens + 1); its metric is decode throughput in GB/s of
 KV bytes read (sum of context lengths x n_kv_heads x head_dim x 2 (K, V) x 2 B).
 The line also carries the other workloads (GQA decode, ragged decode,
-prefill in TFLOP/s) under "per_workload" unless --no-extra.
+prefill in TFLOP/s; for fp16 decode also the graph-captured step) under
+"per_workload" unless --no-extra.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier +
 synchronize on each side, CUDA events on the launching stream; the KV cache
@@ -659,6 +660,10 @@ def main():
                                "steps": n, "device_status": er["status"]}
                 if eb.unit != "GB/s" and peaks[2]:
                     extra[name]["frac_of_sustained_peak"] = ach / peaks[2]
+                if getattr(eb, "graph_setup", None) is not None:
+                    g_ms = time_graph(eb, n, warmup, dctx)
+                    extra[name]["step_graph"] = {
+                        "value": rate(eb.units, g_ms / 1e3, eb.unit), "ms_per_step": g_ms}
                 del eb
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep the headline
