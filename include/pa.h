@@ -191,12 +191,15 @@ int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
  *                total_q = cu_seqlens_q[num_seqs], the rows of q and out
  *   cu_seqlens_q, cu_seqlens_k   device int32 [num_seqs + 1]
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *                (max_blocks_per_seq * 16 must stay within INT32_MAX: the
+ *                kernel bounds L_k by it in int32)
  *   max_seqlen_q host bound on any L_q (sizes the grid; longer sequences
  *                set PA_DEV_BAD_LENGTH and are not computed past it)
  *   out          device fp16 [total_q][n_heads][head_dim]
  *   scale        softmax scale; pass 0 for 1/sqrt(head_dim)
- * Built for head_dim 64 and 128 and any n_heads divisible by n_kv_heads;
- * Q.K^T and P.V run on the tcgen05 tensor cores with TMEM accumulators.
+ * Built for head_dim 64 and 128, any n_heads divisible by n_kv_heads and
+ * num_seqs <= 2048 (PA_ERR_UNSUPPORTED beyond); Q.K^T and P.V run on the
+ * tcgen05 tensor cores with TMEM accumulators.
  */
 int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *cache, int layer,
                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
@@ -216,6 +219,7 @@ int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *cache, int l
  * ranges is finished by an online-softmax merge of its pieces.
  *   q             device fp16 [num_seqs][n_heads][head_dim] (rotated)
  *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ *                 (max_blocks_per_seq * 16 must stay within INT32_MAX)
  *   context_lens  device int32 [num_seqs], each in [1, max_blocks_per_seq*16]
  *                 (others set PA_DEV_BAD_LENGTH and their output is not written)
  *   workspace     device, pa_decode_workspace_bytes(...) bytes, 256-byte
