@@ -167,6 +167,15 @@ def _check_shape(t, shape, name):
                          f"{tuple('*' if w is None else w for w in shape)}")
 
 
+def _table_width(block_tables):
+    """max_blocks_per_seq; the kernels bound lengths by it * 16 in int32."""
+    w = block_tables.shape[1]
+    if w * 16 > 2**31 - 1:
+        raise ValueError(f"block_tables rows of {w} entries: max_blocks_per_seq * 16 "
+                         "must stay within int32")
+    return w
+
+
 def _opt(t, dtype, name, shape):
     return None if t is None else _dev(t, dtype, name, shape)
 
@@ -292,6 +301,7 @@ def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, ma
     B = cu_seqlens_q.shape[0] - 1
     _dev(cu_seqlens_k, torch.int32, "cu_seqlens_k", (B + 1,))
     _dev(block_tables, torch.int32, "block_tables", (B, None))
+    _table_width(block_tables)
     _opt(status, torch.int32, "status", (1,))
     out = _out(out, q)
     _check("pa_prefill_varlen", lib().pa_prefill_varlen(
@@ -316,6 +326,7 @@ def _decode_args(q, block_tables, context_lens, workspace, status):
     _dev(q, torch.float16, "q", (None, None, None))
     B = q.shape[0]
     _dev(block_tables, torch.int32, "block_tables", (B, None))
+    _table_width(block_tables)
     _dev(context_lens, torch.int32, "context_lens", (B,))
     _dev(workspace, torch.uint8, "workspace", (None,))
     _opt(status, torch.int32, "status", (1,))

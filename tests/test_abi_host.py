@@ -233,3 +233,11 @@ def test_c_client_links_and_calls_the_library(libpa, tmp_path):
     assert int(out[7]) == 2 * 4 * 16 * 2 * 64 * 2
     assert out[8] == "2"  # 20 tokens took two of the four blocks
     assert " ".join(out[9:]) == "decode workspace too small"
+
+
+def test_binding_bounds_the_block_table_width():
+    import torch
+    ok = torch.empty(0, (2**31 - 1) // 16, dtype=torch.int32)
+    assert pa._table_width(ok) == (2**31 - 1) // 16
+    with pytest.raises(ValueError):
+        pa._table_width(torch.empty(0, (2**31 - 1) // 16 + 1, dtype=torch.int32))
