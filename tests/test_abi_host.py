@@ -241,3 +241,35 @@ def test_binding_bounds_the_block_table_width():
     assert pa._table_width(ok) == (2**31 - 1) // 16
     with pytest.raises(ValueError):
         pa._table_width(torch.empty(0, (2**31 - 1) // 16 + 1, dtype=torch.int32))
+
+
+def test_prepare_metadata_random_batches_match_oracle(libpa):
+    """Seeded random batches (empty sequences, block-aligned and ragged
+    boundaries, long cached prefixes, permuted tables with padding) give the
+    oracle's metadata bit for bit."""
+    rng = np.random.default_rng(77)
+    for trial in range(60):
+        B = int(rng.integers(1, 12))
+        bs = 16
+        cached = rng.integers(0, 3 * bs, size=B) * rng.integers(0, 2, size=B)
+        cached += rng.integers(0, 5, size=B) * bs * (trial % 3 == 0)
+        new = rng.integers(0, 70, size=B)
+        need = np.maximum((cached + new + bs - 1) // bs, 1)
+        width = int(need.max()) + int(rng.integers(0, 3))
+        perm = rng.permutation(int(need.sum()) + 5).astype(np.int32)
+        table = np.full((B, width), -1, np.int32)
+        at = 0
+        for s in range(B):
+            table[s, :need[s]] = perm[at:at + need[s]]
+            at += need[s]
+        got = pa.prepare_prefill(cached, new, table)
+        want = orc.prefill_metadata(cached, new, table, bs)
+        for key in ("positions", "slot_mapping", "cu_seqlens_q", "cu_seqlens_k"):
+            assert np.array_equal(got[key], want[key]), (trial, key)
+        assert got["max_seqlen_q"] == want["max_seqlen_q"]
+        assert got["max_seqlen_k"] == want["max_seqlen_k"]
+        dec = np.minimum(cached + new, need * bs - 1)  # a position inside the table
+        got = pa.prepare_decode(dec, table)
+        want = orc.decode_metadata(dec, table, bs)
+        for key in ("positions", "slot_mapping", "context_lens"):
+            assert np.array_equal(got[key], want[key]), (trial, key)
