@@ -464,85 +464,197 @@ class DistCtx:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_decode_seq(args):
-    name, s = args
-    from oracle import reference as orc
-    case = W.make_case(name)
+THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _sequence_pool(case, s):
+    """Sequence s's KV blocks alone, as a compact pool (blocks relabelled
+    0..n-1, the same contents), and its one-row block table."""
+    from paged_kv_gqa_rope_gb300.workloads import block_contents
     wl = case.wl
     blocks = [int(b) for b in case.block_tables[s] if b >= 0]
-    cache = W.initial_cache(case, blocks=blocks)
+    pool = np.zeros((2, 1, max(len(blocks), 1), wl.block_size, wl.n_kv_heads, wl.head_dim),
+                    np.float16)
+    for j, b in enumerate(blocks):
+        pool[:, 0, j] = block_contents(wl, b)
+    return pool, np.arange(len(blocks), dtype=np.int32)[None, :]
+
+
+def _oracle_decode_seq(orc, case, s, pool, table):
+    """One sequence's decode step on the oracle: (seconds, KV bytes)."""
+    wl = case.wl
     t0 = time.perf_counter()
-    md = orc.decode_metadata(case.num_cached[s:s + 1], case.block_tables[s:s + 1], wl.block_size)
+    md = orc.decode_metadata(case.num_cached[s:s + 1], table, wl.block_size)
     q = orc.rope_pinned(case.q[s:s + 1], md["positions"], wl.head_dim, wl.rope_theta)
     k = orc.rope_pinned(case.k[s:s + 1], md["positions"], wl.head_dim, wl.rope_theta)
-    orc.kv_write(cache, 0, k, case.v[s:s + 1], md["slot_mapping"])
-    orc.attention_decode(q, cache, 0, case.block_tables[s:s + 1], md["context_lens"],
-                         wl.n_heads, wl.n_kv_heads)
+    orc.kv_write(pool, 0, k, case.v[s:s + 1], md["slot_mapping"])
+    orc.attention_decode(q, pool, 0, table, md["context_lens"], wl.n_heads, wl.n_kv_heads)
     dt = time.perf_counter() - t0
     return dt, (int(case.num_cached[s]) + 1) * wl.n_kv_heads * wl.head_dim * 4
 
 
-def _oracle_prefill_seq(args):
-    name, s = args
-    from oracle import reference as orc
-    case = W.make_case(name)
+def _oracle_prefill_seq(orc, case, s, pool, table):
+    """One sequence's prefill on the oracle: (seconds, FLOPs)."""
     wl = case.wl
-    blocks = [int(b) for b in case.block_tables[s] if b >= 0]
-    cache = W.initial_cache(case, blocks=blocks)
     t0 = time.perf_counter()
     nc, nn = case.num_cached[s:s + 1], case.num_new[s:s + 1]
-    md = orc.prefill_metadata(nc, nn, case.block_tables[s:s + 1], wl.block_size)
+    md = orc.prefill_metadata(nc, nn, table, wl.block_size)
     lo = int(case.num_new[:s].sum())
     hi = lo + int(nn[0])
     q = orc.rope_pinned(case.q[lo:hi], md["positions"], wl.head_dim, wl.rope_theta)
     k = orc.rope_pinned(case.k[lo:hi], md["positions"], wl.head_dim, wl.rope_theta)
-    orc.kv_write(cache, 0, k, case.v[lo:hi], md["slot_mapping"])
-    orc.attention_prefill(q, cache, 0, md["cu_seqlens_q"], md["cu_seqlens_k"],
-                          case.block_tables[s:s + 1], wl.n_heads, wl.n_kv_heads)
+    orc.kv_write(pool, 0, k, case.v[lo:hi], md["slot_mapping"])
+    orc.attention_prefill(q, pool, 0, md["cu_seqlens_q"], md["cu_seqlens_k"], table,
+                          wl.n_heads, wl.n_kv_heads)
     dt = time.perf_counter() - t0
     p, n = int(nc[0]), int(nn[0])
     return dt, 4 * wl.head_dim * wl.n_heads * (n * (p + 1) + n * (n - 1) // 2)
 
 
-def _single_thread_env():
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[v] = "1"
-
-
-def oracle_baseline(name, budget_s=12.0):
-    """Time the oracle on a bounded sample of the workload: whole sequences,
-    one per single-threaded worker process on every host core, cycling
-    through the batch until about `budget_s` CPU-seconds of oracle
-    arithmetic are spent.  Only the oracle's arithmetic of each sequence is
-    on the clock (drawing the synthetic inputs is not)."""
-    import multiprocessing as mp
-    wl = W.WORKLOADS[name]
-    B = W.WORKLOADS[name].batch
-    cores = os.cpu_count() or 1
-    fn = _oracle_prefill_seq if wl.kind == "prefill" else _oracle_decode_seq
-    ctx = mp.get_context("spawn")
-    done, units, cpu_s, nxt = 0, 0, 0.0, 0
-    with ctx.Pool(cores, initializer=_single_thread_env) as pool:
-        pending = []
-        for _ in range(cores):
-            pending.append(pool.apply_async(fn, ((name, nxt % B),)))
-            nxt += 1
-        while pending:
-            dt, u = pending.pop(0).get()
-            done += 1
-            cpu_s += dt
+def _oracle_worker(name, w, stride, inq, outq):
+    """Worker process: owns sequences w, w + stride, ... of workload `name`
+    (their KV blocks drawn once, on first use).  For each request (tag, n)
+    it evaluates the next n of them in turn and answers (tag, oracle
+    seconds, units, n)."""
+    from oracle import reference as orc
+    case = W.make_case(name)
+    fn = _oracle_prefill_seq if case.wl.kind == "prefill" else _oracle_decode_seq
+    mine = list(range(w, case.wl.batch, stride))
+    kept, i = {}, 0
+    while True:
+        msg = inq.get()
+        if msg is None:
+            return
+        tag, n = msg
+        dt_sum, units = 0.0, 0
+        for _ in range(n):
+            s = mine[i % len(mine)]
+            i += 1
+            if s not in kept:
+                kept[s] = _sequence_pool(case, s)
+            dt, u = fn(orc, case, s, *kept[s])
+            dt_sum += dt
             units += u
-            if cpu_s < budget_s:
-                pending.append(pool.apply_async(fn, ((name, nxt % B),)))
-                nxt += 1
-    # `cores` workers run side by side: throughput = units / (CPU-s / cores)
-    used = min(cores, done)
-    wall = cpu_s / used
-    unit = "TFLOP/s" if wl.kind == "prefill" else "GB/s"
-    return dict(value=rate(units, wall, unit), unit=unit, cores=used, kind="oracle",
-                sample=f"{done} sequence evaluations cycling through the {B} sequences of "
-                       f"{name}, one per single-threaded worker, {cpu_s:.1f} CPU-s of "
-                       f"oracle arithmetic")
+        outq.put((tag, dt_sum, units, n))
+
+
+class OracleSampler:
+    """The oracle, as it stands, on bounded samples of a workload: one
+    single-threaded worker process per host core (at most one per sequence),
+    started once.  A step hands every worker `per_worker` whole-sequence
+    evaluations; its throughput is the units done over the oracle seconds
+    spent per worker (the workers run side by side).  Only the oracle's
+    arithmetic is on the clock (drawing the synthetic inputs is not)."""
+
+    def __init__(self, name):
+        import multiprocessing as mp
+        self.name = name
+        self.B = W.WORKLOADS[name].batch
+        self.cores = max(1, min(os.cpu_count() or 1, self.B))
+        ctx = mp.get_context("spawn")
+        # The workers import numpy before any initializer runs: the thread
+        # limits go in through the environment they inherit.
+        saved = {v: os.environ.get(v) for v in THREAD_VARS}
+        os.environ.update({v: "1" for v in THREAD_VARS})
+        try:
+            self.inq = [ctx.Queue() for _ in range(self.cores)]
+            self.outq = ctx.Queue()
+            self.procs = [ctx.Process(target=_oracle_worker,
+                                      args=(name, w, self.cores, self.inq[w], self.outq),
+                                      daemon=True) for w in range(self.cores)]
+            for p in self.procs:
+                p.start()
+        finally:
+            for v, x in saved.items():
+                if x is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = x
+        self.items = 0
+        self.item_s = None  # mean oracle seconds per item, once measured
+
+    def step(self, per_worker):
+        """Every worker evaluates `per_worker` sequences.  Returns (units,
+        oracle seconds per worker, items)."""
+        for q in self.inq:
+            q.put((0, per_worker))
+        cpu_s, units, n = 0.0, 0, 0
+        for _ in range(self.cores):
+            _, dt, u, k = self.outq.get(timeout=1800)
+            cpu_s, units, n = cpu_s + dt, units + u, n + k
+        self.items += n
+        self.item_s = cpu_s / n
+        return units, cpu_s / self.cores, n
+
+    def samples(self, count, per_sample):
+        """`count` independent samples of `per_sample` sequences each, sample
+        i on worker i mod cores, all in flight together.  Returns per sample
+        (units, oracle seconds), in order."""
+        for i in range(count):
+            self.inq[i % self.cores].put((i, per_sample))
+        out = [None] * count
+        for _ in range(count):
+            tag, dt, u, _ = self.outq.get(timeout=1800)
+            out[tag] = (u, dt)
+        self.items += count * per_sample
+        return out
+
+    def per_worker_for(self, wall_s):
+        """Items per worker that take about `wall_s` seconds."""
+        return max(1, int(wall_s / self.item_s)) if self.item_s else 1
+
+    def close(self):
+        for q in self.inq:
+            q.put(None)
+        for p in self.procs:
+            p.join(30)
+            if p.is_alive():
+                p.terminate()
+
+
+def oracle_baseline(name, budget_s=15.0):
+    """The `cpu_baseline` key: one sample of about `budget_s` CPU-seconds of
+    oracle arithmetic (after two untimed rounds: the first draws the inputs,
+    the second, warm, sizes the sample)."""
+    smp = OracleSampler(name)
+    try:
+        smp.step(1)
+        smp.step(1)
+        k = smp.per_worker_for(budget_s / smp.cores)
+        units, wall, n = smp.step(k)
+    finally:
+        smp.close()
+    unit = "TFLOP/s" if W.WORKLOADS[name].kind == "prefill" else "GB/s"
+    return dict(value=rate(units, wall, unit), unit=unit, cores=smp.cores, kind="oracle",
+                sample=f"{n} sequence evaluations cycling through the {smp.B} sequences of "
+                       f"{name}, {k} per single-threaded worker, {wall * smp.cores:.1f} CPU-s "
+                       f"of oracle arithmetic")
+
+
+def reference_arm(name, steps, warmup, wall_budget_s=45.0):
+    """`--impl reference`: the oracle timed over `warmup` untimed and `steps`
+    timed steps.  A step is a bounded sample (whole sequences on one
+    single-threaded worker) and its value is that worker's rate times the
+    number of workers, which run side by side; the samples are independent,
+    so the workers take them in turn, and each is sized so that the whole
+    run spends about `wall_budget_s` seconds on every worker (at least one
+    sequence per sample).  Returns (median value, unit, info)."""
+    smp = OracleSampler(name)
+    unit = "TFLOP/s" if W.WORKLOADS[name].kind == "prefill" else "GB/s"
+    try:
+        smp.step(1)  # draws every worker's inputs; also the per-item estimate
+        k = smp.per_worker_for(wall_budget_s * smp.cores / (steps + warmup))
+        res = smp.samples(warmup + steps, k)[warmup:]
+    finally:
+        smp.close()
+    vals = [rate(u, dt / smp.cores, unit) for u, dt in res]
+    cpu = sum(dt for _, dt in res)
+    info = dict(cores=smp.cores, kind="oracle",
+                sample=f"per step {k} sequence evaluation(s) on one of {smp.cores} "
+                       f"single-threaded workers (taken in turn, value = its rate x "
+                       f"{smp.cores}), cycling through the {smp.B} sequences of {name}; "
+                       f"{cpu:.1f} CPU-s of oracle arithmetic over {steps} timed steps")
+    return float(np.median(vals)), unit, info
 
 
 # ---------------------------------------------------------------- main
@@ -567,17 +679,13 @@ def main():
         if dctx.rank != 0:
             return
         steps = args.steps or 3
-        vals = []
-        for _ in range(steps):
-            vals.append(oracle_baseline(args.workload, budget_s=8.0))
-        v = float(np.median([x["value"] for x in vals]))
-        unit = vals[0]["unit"]
+        v, unit, info = reference_arm(args.workload, steps, warmup)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit,
-                "n_gpus": args.gpus, "steps": steps, "warmup": 0,
+                "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
                 "config": {"workload": args.workload},
-                "cpu_baseline": dict(vals[0], value=v),
+                "cpu_baseline": dict(info, value=v, unit=unit),
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
