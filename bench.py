@@ -573,6 +573,17 @@ class OracleSampler:
         self.items = 0
         self.item_s = None  # mean oracle seconds per item, once measured
 
+    def _get(self):
+        """The next answer; raises at once if a worker has died."""
+        import queue
+        while True:
+            try:
+                return self.outq.get(timeout=2.0)
+            except queue.Empty:
+                dead = [p.exitcode for p in self.procs if p.exitcode is not None]
+                if dead:
+                    raise RuntimeError(f"oracle worker exited with code {dead[0]}")
+
     def step(self, per_worker):
         """Every worker evaluates `per_worker` sequences.  Returns (units,
         oracle seconds per worker, items)."""
@@ -580,7 +591,7 @@ class OracleSampler:
             q.put((0, per_worker))
         cpu_s, units, n = 0.0, 0, 0
         for _ in range(self.cores):
-            _, dt, u, k = self.outq.get(timeout=1800)
+            _, dt, u, k = self._get()
             cpu_s, units, n = cpu_s + dt, units + u, n + k
         self.items += n
         self.item_s = cpu_s / n
@@ -594,7 +605,7 @@ class OracleSampler:
             self.inq[i % self.cores].put((i, per_sample))
         out = [None] * count
         for _ in range(count):
-            tag, dt, u, _ = self.outq.get(timeout=1800)
+            tag, dt, u, _ = self._get()
             out[tag] = (u, dt)
         self.items += count * per_sample
         return out
