@@ -10,17 +10,21 @@ against its whole cache (pa_decode).  For the prefill workload: RoPE + append
 of the new tokens and varlen causal prefill reading the cached prefix
 through block_tables (pa_prefill_varlen).
 
-The headline workload is the Llama-2-7B-shaped MHA decode (32 heads, d=128,
-batch 32, 2048 cached tokens + 1); its metric is decode throughput in GB/s of
-KV bytes read (sum of context lengths x n_kv_heads x head_dim x 2 (K, V) x 2 B).
-The line also carries the other workloads (GQA decode, ragged decode,
-prefill in TFLOP/s; for fp16 decode also the graph-captured step) under
-"per_workload" unless --no-extra.
+The headline workload is the Llama-2-70B-shaped GQA decode (64 Q heads over
+8 KV heads, d=128, batch 32, 4096 cached tokens + 1); its metric is decode
+throughput in GB/s of KV bytes read (sum of context lengths x n_kv_heads x
+head_dim x 2 (K, V) x 2 B).  The line also carries the other workloads (MHA
+decode, ragged GQA decode, prefill in TFLOP/s, the int8 cache; for fp16
+decode also the graph-captured step, and for every workload the RoPE/append
+kernel's own time and bandwidth) under "per_workload" unless --no-extra; the
+ragged GQA decode there is instrumented like the headline (roofline with
+ncu traffic, e2e, cpu_baseline).
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier +
-synchronize on each side, CUDA events on the launching stream; the KV cache
-(>= 1 GB) is larger than the 129 MB L2, so nothing is served from L2 across
-steps.  Per-kernel durations of the dominant kernel come from events around
+synchronize on each side, CUDA events on the launching stream; the KV bytes
+a step reads (0.54 to 5.0 GB; 0.28 GB and up for the int8 cache) are larger
+than the 129 MB L2 (inputs larger than L2; no flush between steps).  The
+line gives the mean and the median step time.  Per-kernel durations of the dominant kernel come from events around
 its launches inside the same timed loop.  `e2e` repeats the step through the
 library's calls with the step's inputs copied from pinned host memory (one
 copy of a buffer that holds them all) and the output copied back inside the
@@ -56,7 +60,7 @@ if ROOT not in sys.path:
 
 from paged_kv_gqa_rope_gb300 import workloads as W  # noqa: E402
 
-HEADLINE = "mha_decode_7b"
+HEADLINE = "gqa_decode_70b"
 METRIC = "paged GQA decode KV GB/s (% of HBM peak); prefill attention TFLOP/s (% peak)"
 
 
@@ -84,6 +88,23 @@ def kv_bytes_i8(case) -> int:
     wl = case.wl
     ctx = case.num_cached.astype(np.int64) + 1
     return int(ctx.sum()) * wl.n_kv_heads * (wl.head_dim + 4) * 2
+
+
+def rope_bytes(case) -> int:
+    """Algorithmic bytes of pa_rope_kv_write: Q, K, V of the new tokens read;
+    rotated Q and K written back in place; K and V written into the pool
+    (the cos/sin table rows are not counted)."""
+    wl = case.wl
+    T, H, Hk, d = case.total_new, wl.n_heads, wl.n_kv_heads, wl.head_dim
+    return T * (H + 2 * Hk) * d * 2 + T * (H + 3 * Hk) * d * 2
+
+
+def rope_bytes_i8(case) -> int:
+    """pa_rope_kv_write_i8: the same reads and in-place writes; K and V go
+    into the pool as int8 codes plus one fp32 scale per (token, KV head)."""
+    wl = case.wl
+    T, H, Hk, d = case.total_new, wl.n_heads, wl.n_kv_heads, wl.head_dim
+    return T * (H + 2 * Hk) * d * 2 + T * (H + Hk) * d * 2 + 2 * T * Hk * (d + 4)
 
 
 def prefill_flops(case) -> int:
@@ -187,11 +208,13 @@ class PackedInputs:
 
 
 class DecodeBench:
-    def __init__(self, name, dev, int8=False):
+    rope_kernel = "rope_kv_write_kernel"
+
+    def __init__(self, name, dev, int8=False, batch=None):
         import torch
         from paged_kv_gqa_rope_gb300 import pa
         self.pa, self.torch = pa, torch
-        case = W.make_case(name)
+        case = W.make_case(name, batch=batch)
         self.case = case
         wl = case.wl
         md = pa.prepare_decode(case.num_cached, case.block_tables)
@@ -210,18 +233,23 @@ class DecodeBench:
         self.status = pa.new_status(dev)
         self.units = kv_bytes(case)
         self.unit = "GB/s"
+        self.rope_units = rope_bytes(case)
         self.launches_per_step = 2
 
     def step(self, ev=None):
+        """One step; `ev` = three CUDA events recorded before the RoPE/append
+        kernel, between it and the attention kernel, and after that."""
         pa, d, wl = self.pa, self.d, self.case.wl
+        if ev is not None:
+            ev[0].record()
         pa.rope_kv_write(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
                          self.cache, status=self.status)
         if ev is not None:
-            ev[0].record()
+            ev[1].record()
         pa.decode(d["q"], self.cache, d["bt"], d["ctx"], self.ws, wl.n_kv_heads, out=self.out,
                   status=self.status)
         if ev is not None:
-            ev[1].record()
+            ev[2].record()
 
     def e2e_setup(self):
         """Inputs from pinned host memory (one copy), the step, output back
@@ -269,8 +297,8 @@ class DecodeBench:
 class DecodeI8Bench(DecodeBench):
     """The same decode step against the int8 cache (codes + scales)."""
 
-    def __init__(self, name, dev):
-        super().__init__(name, dev, int8=True)
+    def __init__(self, name, dev, batch=None):
+        super().__init__(name, dev, int8=True, batch=batch)
         import torch
         pa, case, wl = self.pa, self.case, self.case.wl
         self.cache8 = pa.CacheI8(1, case.num_blocks, wl.n_kv_heads, wl.head_dim, device=dev)
@@ -281,30 +309,40 @@ class DecodeI8Bench(DecodeBench):
         self.cache8.scales.copy_(torch.rand(self.cache8.scales.shape, generator=g, device=dev) /
                                  64 + 1e-3)
         self.units = kv_bytes_i8(case)
+        self.rope_units = rope_bytes_i8(case)
 
     def step(self, ev=None):
+        """One step; `ev` = three CUDA events recorded before the RoPE/append
+        kernel, between it and the attention kernel, and after that."""
         pa, d, wl = self.pa, self.d, self.case.wl
+        if ev is not None:
+            ev[0].record()
         pa.rope_kv_write_i8(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
                             self.cache8, status=self.status)
         if ev is not None:
-            ev[0].record()
+            ev[1].record()
         pa.decode_i8(d["q"], self.cache8, d["bt"], d["ctx"], self.ws, wl.n_kv_heads, out=self.out,
                      status=self.status)
         if ev is not None:
-            ev[1].record()
+            ev[2].record()
 
     def kernel_name(self):
         return "decode_kernel (int8 cache)"
+
+    rope_kernel = "rope_kv_write_i8_kernel"
 
     graph_setup = None  # the captured step is the fp16 cache's
 
 
 class PrefillBench:
-    def __init__(self, name, dev):
+    rope_kernel = "rope_kv_write_kernel"
+    graph_setup = None
+
+    def __init__(self, name, dev, batch=None):
         import torch
         from paged_kv_gqa_rope_gb300 import pa
         self.pa, self.torch = pa, torch
-        case = W.make_case(name)
+        case = W.make_case(name, batch=batch)
         self.case = case
         wl = case.wl
         md = pa.prepare_prefill(case.num_cached, case.num_new, case.block_tables)
@@ -321,18 +359,23 @@ class PrefillBench:
         self.status = pa.new_status(dev)
         self.units = prefill_flops(case)
         self.unit = "TFLOP/s"
+        self.rope_units = rope_bytes(case)
         self.launches_per_step = 2
 
     def step(self, ev=None):
+        """One step; `ev` = three CUDA events recorded before the RoPE/append
+        kernel, between it and the attention kernel, and after that."""
         pa, d, wl = self.pa, self.d, self.case.wl
+        if ev is not None:
+            ev[0].record()
         pa.rope_kv_write(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table,
                          self.cache, status=self.status)
         if ev is not None:
-            ev[0].record()
+            ev[1].record()
         pa.prefill_varlen(d["q"], self.cache, d["cuq"], d["cuk"], d["bt"], self.md["max_seqlen_q"],
                           wl.n_kv_heads, out=self.out, status=self.status)
         if ev is not None:
-            ev[1].record()
+            ev[2].record()
 
     def e2e_setup(self):
         torch = self.torch
@@ -351,52 +394,80 @@ class PrefillBench:
         return "prefill_kernel"
 
 
-def make_bench(name, dev):
-    return (PrefillBench if W.WORKLOADS[name].kind == "prefill" else DecodeBench)(name, dev)
+def make_bench(name, dev, int8=False, batch=None):
+    if int8:
+        return DecodeI8Bench(name, dev, batch=batch)
+    return (PrefillBench if W.WORKLOADS[name].kind == "prefill" else DecodeBench)(name, dev,
+                                                                                  batch=batch)
 
 
-def committed_traffic(kernel, workload):
-    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
-    summary, or None when that capture was of another workload or of an
-    older version of the kernel's source."""
+def committed_traffic(kernel, workload, units=None):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from
+    the committed ncu summaries, or None when there is no capture of that
+    kernel on that workload made from the kernel's current source.  A
+    capture of a smaller case of the same workload (fewer sequences) is
+    scaled to a full launch by the algorithmic units (`units` = a full
+    launch's), since the traffic of these kernels grows in proportion."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+            recs = json.load(f)
     except Exception:
         return None
-    if rec["workload"] != workload or not sha.startswith(rec["sha256_prefix"]):
-        return None
-    return rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    for rec in recs if isinstance(recs, list) else []:
+        if not isinstance(rec, dict) or rec.get("kernel") != kernel or \
+                rec.get("workload") != workload:
+            continue
+        try:
+            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()
+        except OSError:
+            return None
+        if not sha.startswith(rec["sha256_prefix"]):
+            return None
+        t = rec["dram_bytes_read"] + rec["dram_bytes_write"]
+        cap = rec.get("units_captured")
+        if cap and units and cap != units:
+            t = int(round(t * units / cap))
+        return t
+    return None
 
 
 def rate(units, seconds, unit):
     return units / seconds / (1e9 if unit == "GB/s" else 1e12)
 
 
-def time_bench(b, steps, warmup, dist_ctx, clocks=None):
-    """Returns dict: ms_per_step (max over ranks), kernel_ms (mean per launch)."""
+def time_bench(b, steps, warmup, dist_ctx):
+    """Times `steps` steps after `warmup` untimed ones.  Returns (ms per step
+    over the whole timed region, max over ranks), the mean and median of
+    each step's own duration, of the attention kernel's and of the
+    RoPE/append kernel's (CUDA events on the launching stream around every
+    launch), and the device status word."""
     torch = b.torch
     for _ in range(warmup):
         b.step()
     torch.cuda.synchronize()
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    kev = [(E(), E(), E()) for _ in range(steps)]
+    stop = E()
     dist_ctx.barrier()
     torch.cuda.synchronize()
-    start.record()
     for i in range(steps):
         b.step(kev[i])
     stop.record()
     torch.cuda.synchronize()
     dist_ctx.barrier()
-    ms = start.elapsed_time(stop) / steps
-    kms = sum(a.elapsed_time(z) for a, z in kev) / steps
+    ms = kev[0][0].elapsed_time(stop) / steps
+    starts = [e[0] for e in kev] + [stop]
+    step_ms = [starts[i].elapsed_time(starts[i + 1]) for i in range(steps)]
+    kern = [z.elapsed_time(w) for _, z, w in kev]
+    rope = [a.elapsed_time(z) for a, z, _ in kev]
     st = int(b.status.item())
-    return dict(ms=dist_ctx.max(ms), kernel_ms=dist_ctx.max(kms), status=st)
+    return dict(ms=dist_ctx.max(ms), ms_median=dist_ctx.max(float(np.median(step_ms))),
+                kernel_ms=dist_ctx.max(float(np.mean(kern))),
+                kernel_ms_median=dist_ctx.max(float(np.median(kern))),
+                rope_ms=dist_ctx.max(float(np.mean(rope))),
+                rope_ms_median=dist_ctx.max(float(np.median(rope))), status=st)
 
 
 def time_e2e(b, steps, warmup, dist_ctx):
@@ -515,7 +586,7 @@ def _oracle_worker(name, w, stride, inq, outq):
     """Worker process: owns sequences w, w + stride, ... of workload `name`
     (their KV blocks drawn once, on first use).  For each request (tag, n)
     it evaluates the next n of them in turn and answers (tag, oracle
-    seconds, units, n)."""
+    seconds, units, n, w)."""
     from oracle import reference as orc
     case = W.make_case(name)
     fn = _oracle_prefill_seq if case.wl.kind == "prefill" else _oracle_decode_seq
@@ -535,22 +606,28 @@ def _oracle_worker(name, w, stride, inq, outq):
             dt, u = fn(orc, case, s, *kept[s])
             dt_sum += dt
             units += u
-        outq.put((tag, dt_sum, units, n))
+        outq.put((tag, dt_sum, units, n, w))
 
 
 class OracleSampler:
     """The oracle, as it stands, on bounded samples of a workload: one
-    single-threaded worker process per host core (at most one per sequence),
-    started once.  A step hands every worker `per_worker` whole-sequence
-    evaluations; its throughput is the units done over the oracle seconds
-    spent per worker (the workers run side by side).  Only the oracle's
-    arithmetic is on the clock (drawing the synthetic inputs is not)."""
+    single-threaded worker process per host core (at most one per sequence;
+    `cores` caps the count), started once.  A step hands every worker
+    `per_worker` whole-sequence evaluations; its throughput is the units
+    done over the oracle seconds spent per worker (the workers run side by
+    side).  Only the oracle's arithmetic is on the clock (drawing the
+    synthetic inputs is not)."""
 
-    def __init__(self, name):
+    # the first answer of a worker includes drawing its inputs and starting
+    # the interpreter: it gets this long; later ones ten times their
+    # expected oracle time, but at least two minutes
+    FIRST_LIMIT_S = 1800.0
+
+    def __init__(self, name, cores=None):
         import multiprocessing as mp
         self.name = name
         self.B = W.WORKLOADS[name].batch
-        self.cores = max(1, min(os.cpu_count() or 1, self.B))
+        self.cores = max(1, min(cores or os.cpu_count() or 1, self.B))
         ctx = mp.get_context("spawn")
         # The workers import numpy before any initializer runs: the thread
         # limits go in through the environment they inherit.
@@ -572,26 +649,47 @@ class OracleSampler:
                     os.environ[v] = x
         self.items = 0
         self.item_s = None  # mean oracle seconds per item, once measured
+        self.pending = [0] * self.cores  # requests each worker has not answered
 
-    def _get(self):
-        """The next answer; raises at once if a worker has died."""
+    def _limit(self, items_per_worker):
+        if self.item_s is None:
+            return self.FIRST_LIMIT_S
+        return max(120.0, 10.0 * self.item_s * items_per_worker)
+
+    def _put(self, w, tag, n):
+        self.pending[w] += 1
+        self.inq[w].put((tag, n))
+
+    def _get(self, deadline, limit):
+        """The next answer.  Raises at once if a worker has died, and once
+        time.monotonic() passes `deadline`, naming the workers that still
+        owe an answer."""
         import queue
         while True:
             try:
-                return self.outq.get(timeout=2.0)
+                ans = self.outq.get(timeout=2.0)
+                self.pending[ans[4]] -= 1
+                return ans
             except queue.Empty:
-                dead = [p.exitcode for p in self.procs if p.exitcode is not None]
+                dead = [w for w, p in enumerate(self.procs) if p.exitcode is not None]
                 if dead:
-                    raise RuntimeError(f"oracle worker exited with code {dead[0]}")
+                    raise RuntimeError(f"oracle worker(s) {dead} exited with code "
+                                       f"{self.procs[dead[0]].exitcode}")
+                if time.monotonic() > deadline:
+                    late = [w for w, k in enumerate(self.pending) if k > 0]
+                    raise RuntimeError(f"oracle worker(s) {late} gave no answer within "
+                                       f"{limit:.0f} s")
 
     def step(self, per_worker):
         """Every worker evaluates `per_worker` sequences.  Returns (units,
         oracle seconds per worker, items)."""
-        for q in self.inq:
-            q.put((0, per_worker))
+        limit = self._limit(per_worker)
+        deadline = time.monotonic() + limit
+        for w in range(self.cores):
+            self._put(w, 0, per_worker)
         cpu_s, units, n = 0.0, 0, 0
         for _ in range(self.cores):
-            _, dt, u, k = self._get()
+            _, dt, u, k, _ = self._get(deadline, limit)
             cpu_s, units, n = cpu_s + dt, units + u, n + k
         self.items += n
         self.item_s = cpu_s / n
@@ -601,11 +699,13 @@ class OracleSampler:
         """`count` independent samples of `per_sample` sequences each, sample
         i on worker i mod cores, all in flight together.  Returns per sample
         (units, oracle seconds), in order."""
+        limit = self._limit(-(-count // self.cores) * per_sample)
+        deadline = time.monotonic() + limit
         for i in range(count):
-            self.inq[i % self.cores].put((i, per_sample))
+            self._put(i % self.cores, i, per_sample)
         out = [None] * count
         for _ in range(count):
-            tag, dt, u, _ = self._get()
+            tag, dt, u, _, _ = self._get(deadline, limit)
             out[tag] = (u, dt)
         self.items += count * per_sample
         return out
@@ -623,11 +723,12 @@ class OracleSampler:
                 p.terminate()
 
 
-def oracle_baseline(name, budget_s=15.0):
+def oracle_baseline(name, budget_s=15.0, cores=None):
     """The `cpu_baseline` key: one sample of about `budget_s` CPU-seconds of
     oracle arithmetic (after two untimed rounds: the first draws the inputs,
-    the second, warm, sizes the sample)."""
-    smp = OracleSampler(name)
+    the second, warm, sizes the sample), on one single-threaded worker per
+    host core, or on `cores` of them."""
+    smp = OracleSampler(name, cores=cores)
     try:
         smp.step(1)
         smp.step(1)
@@ -670,12 +771,88 @@ def reference_arm(name, steps, warmup, wall_budget_s=45.0):
 
 # ---------------------------------------------------------------- main
 
+def workload_config(name, batch, int8=False, world=1):
+    """The `config` object of a line: the workload and its shape."""
+    wl = W.WORKLOADS[name]
+    return {"workload": name, "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
+            "head_dim": wl.head_dim, "block_size": wl.block_size, "batch": batch,
+            "kv_cache": "int8 codes + fp32 scales" if int8 else "fp16",
+            "l2": "inputs larger than L2 (KV bytes or prefill Q/K/V/O per step > 129 MB); "
+                  "no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+INPUT_NOTE = ("every timed step runs on the same device buffers: RoPE rotates the step's "
+              "q/k in place again each step (its cost does not depend on the values); "
+              "the int8 cache of the timed int8 steps holds seeded random codes and "
+              "scales, not the quantised fp16 history (decode cost does not depend on "
+              "the code values)")
+
+
+def measure(b, name, steps, warmup, dctx, peaks, with_e2e=True, with_graph=True):
+    """Time workload `name` on bench `b`: the step (mean and median), the
+    dominant kernel against its roofline, the RoPE/append kernel on its own,
+    and optionally the end-to-end step (host I/O inside the timed region)
+    and the graph-captured decode step."""
+    r = time_bench(b, steps, warmup, dctx)
+    world = dctx.world
+    if b.unit == "GB/s":
+        peak, bound = peaks[0], "hbm"
+    else:
+        peak, bound = peaks[1], "tensor"
+    achieved = rate(b.units, r["kernel_ms"] / 1e3, b.unit)
+    rope_gbs = rate(b.rope_units, r["rope_ms"] / 1e3, "GB/s")
+    out = {
+        "value": rate(b.units * world, r["ms"] / 1e3, b.unit), "unit": b.unit,
+        "ms_per_step": r["ms"], "ms_per_step_median": r["ms_median"], "steps": steps,
+        "roofline": {"bound": bound, "kernel": b.kernel_name(), "achieved": achieved,
+                     "peak": peak, "peak_source": peaks[3], "unit": b.unit,
+                     "frac": achieved / peak,
+                     "traffic": committed_traffic(b.kernel_name(), name, b.units),
+                     "kernel_ms": r["kernel_ms"], "kernel_ms_median": r["kernel_ms_median"],
+                     "units_per_launch": b.units},
+        "rope_kv_write": {"kernel": b.rope_kernel, "ms": r["rope_ms"],
+                          "ms_median": r["rope_ms_median"], "bytes_per_launch": b.rope_units,
+                          "GB/s": rope_gbs, "frac_of_hbm": rope_gbs / peaks[0]},
+        "device_status": r["status"],
+    }
+    if b.unit != "GB/s" and peaks[2]:
+        # the same against the sustained cuBLAS figure, which was measured
+        # with the clocks held down by the power cap
+        out["roofline_sustained"] = {"peak": peaks[2], "frac": achieved / peaks[2],
+                                     "note": "peak of a seconds-long cuBLAS loop at "
+                                             "power-capped clocks; this kernel runs at "
+                                             "the clocks in 'clocks'"}
+    if with_e2e:
+        e2e_ms, h2d, d2h = time_e2e(b, max(10, steps // 4), warmup, dctx)
+        out["e2e"] = {"value": rate(b.units * world, e2e_ms / 1e3, b.unit), "unit": b.unit,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": e2e_ms}
+    if with_graph and getattr(b, "graph_setup", None) is not None:
+        g_ms = time_graph(b, steps, warmup, dctx)
+        out["step_graph"] = {"value": rate(b.units * world, g_ms / 1e3, b.unit),
+                             "unit": b.unit, "ms_per_step": g_ms, "steps": steps,
+                             "kernels_per_step": 2,
+                             "how": "pa_step_graph: RoPE/append + decode captured once "
+                                    "(programmatic dependent launch between them), replayed"}
+    return out
+
+
+# workloads reported under per_workload, and whether each gets the headline's
+# whole instrumentation (e2e, cpu_baseline)
+EXTRA = (("mha_decode_7b", False), ("ragged_decode", True), ("gqa_decode_70b", False),
+         ("prefill_13b", False), ("mha_decode_7b:int8", False), ("gqa_decode_70b:int8", False),
+         ("ragged_decode:int8", False))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer sequences of the same workload (profiling a smaller case)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -685,6 +862,8 @@ def main():
     warmup = max(3, args.warmup)
     dctx = DistCtx()
     peaks = load_peaks()
+    wl = W.WORKLOADS[args.workload]
+    batch = wl.batch if args.batch is None else min(args.batch, wl.batch)
 
     if args.impl == "reference":
         if dctx.rank != 0:
@@ -694,8 +873,8 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit,
                 "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f64", "data": "synthetic",
-                "config": {"workload": args.workload},
+                "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
+                "config": workload_config(args.workload, batch, args.int8, args.gpus),
                 "cpu_baseline": dict(info, value=v, unit=unit),
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -707,49 +886,47 @@ def main():
     dev = f"cuda:{dctx.local}"
     from paged_kv_gqa_rope_gb300 import pa
     pa.lib()
-    wl = W.WORKLOADS[args.workload]
     if args.int8 and wl.kind != "decode":
         raise SystemExit("--int8 applies to decode workloads")
-    b = DecodeI8Bench(args.workload, dev) if args.int8 else make_bench(args.workload, dev)
+    b = make_bench(args.workload, dev, int8=args.int8, batch=args.batch)
     steps = args.steps or (4000 if wl.kind != "prefill" else 2000)
     with ClockSampler(dctx.local) as clk:
         r = time_bench(b, steps, warmup, dctx)
-    e2e_ms, h2d, d2h = time_e2e(b, max(10, steps // 4), warmup, dctx)
+    clocks = clk.summary()
+    # the timed loop above is the headline; e2e and the step graph follow it
     value = rate(b.units * dctx.world, r["ms"] / 1e3, b.unit)
     achieved = rate(b.units, r["kernel_ms"] / 1e3, b.unit)
-    if b.unit == "GB/s":
-        peak, bound, punit, pkind = peaks[0], "hbm", "GB/s", peaks[3]
-    else:
-        peak, bound, punit, pkind = peaks[1], "tensor", "TFLOP/s", peaks[3]
+    peak, bound = (peaks[0], "hbm") if b.unit == "GB/s" else (peaks[1], "tensor")
+    e2e_ms, h2d, d2h = time_e2e(b, max(10, steps // 4), warmup, dctx)
+    rope_gbs = rate(b.rope_units, r["rope_ms"] / 1e3, "GB/s")
     line = {
         "metric": METRIC, "value": value, "unit": b.unit, "n_gpus": dctx.world,
-        "steps": steps, "warmup": warmup, "ms_per_step": r["ms"], "higher_is_better": True,
+        "steps": steps, "warmup": warmup, "ms_per_step": r["ms"],
+        "ms_per_step_median": r["ms_median"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16 (fp32 accumulate)",
         "data": "synthetic (seeded; shapes of the pages' workloads)",
-        "config": {"workload": args.workload, "n_heads": wl.n_heads,
-                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
-                   "block_size": wl.block_size, "batch": len(b.case.num_new),
-                   "kv_cache": "int8 codes + fp32 scales" if args.int8 else "fp16",
-                   "l2": "inputs larger than L2 (KV cache >= 1 GB per step)",
-                   "parallelism": "replicas" if dctx.world > 1 else "single GPU"},
+        "inputs": INPUT_NOTE,
+        "config": workload_config(args.workload, batch, args.int8, dctx.world),
         "roofline": {"bound": bound, "kernel": b.kernel_name(), "achieved": achieved,
-                     "peak": peak, "peak_source": pkind, "unit": punit,
+                     "peak": peak, "peak_source": peaks[3], "unit": b.unit,
                      "frac": achieved / peak,
-                     "traffic": committed_traffic(b.kernel_name(), args.workload),
-                     "kernel_ms": r["kernel_ms"]},
+                     "traffic": committed_traffic(b.kernel_name(), args.workload, b.units),
+                     "kernel_ms": r["kernel_ms"], "kernel_ms_median": r["kernel_ms_median"],
+                     "units_per_launch": b.units},
         "e2e": {"value": rate(b.units * dctx.world, e2e_ms / 1e3, b.unit), "unit": b.unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "rope_kv_write": {"kernel": b.rope_kernel, "ms": r["rope_ms"],
+                          "ms_median": r["rope_ms_median"], "bytes_per_launch": b.rope_units,
+                          "GB/s": rope_gbs, "frac_of_hbm": rope_gbs / peaks[0]},
         "gpu_launches": b.launches_per_step * steps,
-        # (tensor-bound lines) the same against the sustained cuBLAS figure,
-        # which was measured with the clocks held down by the power cap
-        **({"roofline_sustained": {"peak": peaks[2], "frac": achieved / peaks[2],
-                                   "note": "peak of a seconds-long cuBLAS loop at "
-                                           "power-capped clocks; this kernel runs at "
-                                           "the clocks in 'clocks'"}}
-           if b.unit != "GB/s" and peaks[2] else {}),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "device_status": r["status"],
     }
+    if b.unit != "GB/s" and peaks[2]:
+        line["roofline_sustained"] = {"peak": peaks[2], "frac": achieved / peaks[2],
+                                      "note": "peak of a seconds-long cuBLAS loop at "
+                                              "power-capped clocks; this kernel runs at "
+                                              "the clocks in 'clocks'"}
     if getattr(b, "graph_setup", None) is not None:
         g_ms = time_graph(b, steps, warmup, dctx)
         line["step_graph"] = {"value": rate(b.units * dctx.world, g_ms / 1e3, b.unit),
@@ -757,32 +934,21 @@ def main():
                               "kernels_per_step": 2,
                               "how": "pa_step_graph: RoPE/append + decode captured once "
                                      "(programmatic dependent launch between them), replayed"}
-    if not args.no_extra and dctx.world == 1:
+    full_extra = []
+    if not args.no_extra and dctx.world == 1 and args.batch is None:
         extra = {}
         del b
         torch.cuda.empty_cache()
-        for name in ("gqa_decode_70b", "ragged_decode", "prefill_13b", "mha_decode_7b:int8",
-                     "gqa_decode_70b:int8", "ragged_decode:int8"):
+        for name, full in EXTRA:
             if name == args.workload + (":int8" if args.int8 else ""):
                 continue
             try:
                 base, _, kind = name.partition(":")
-                eb = DecodeI8Bench(base, dev) if kind == "int8" else make_bench(base, dev)
+                eb = make_bench(base, dev, int8=(kind == "int8"))
                 n = 1000 if eb.unit == "GB/s" else 400
-                er = time_bench(eb, n, warmup, dctx)
-                ach = rate(eb.units, er["kernel_ms"] / 1e3, eb.unit)
-                pk = peaks[0] if eb.unit == "GB/s" else peaks[1]
-                extra[name] = {"value": rate(eb.units, er["ms"] / 1e3, eb.unit),
-                               "unit": eb.unit, "ms_per_step": er["ms"],
-                               "kernel": eb.kernel_name(), "kernel_ms": er["kernel_ms"],
-                               "kernel_achieved": ach, "frac_of_peak": ach / pk,
-                               "steps": n, "device_status": er["status"]}
-                if eb.unit != "GB/s" and peaks[2]:
-                    extra[name]["frac_of_sustained_peak"] = ach / peaks[2]
-                if getattr(eb, "graph_setup", None) is not None:
-                    g_ms = time_graph(eb, n, warmup, dctx)
-                    extra[name]["step_graph"] = {
-                        "value": rate(eb.units, g_ms / 1e3, eb.unit), "ms_per_step": g_ms}
+                extra[name] = measure(eb, base, n, warmup, dctx, peaks, with_e2e=full)
+                if full:
+                    full_extra.append(name)
                 del eb
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep the headline
@@ -790,6 +956,10 @@ def main():
         line["per_workload"] = extra
     if dctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(args.workload)
+        line["cpu_baseline"]["single_thread"] = oracle_baseline(args.workload, budget_s=6.0,
+                                                                cores=1)
+        for name in full_extra:
+            line["per_workload"][name]["cpu_baseline"] = oracle_baseline(name)
     if dctx.rank == 0:
         print(json.dumps(line))
 

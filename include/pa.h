@@ -251,16 +251,24 @@ int pa_decode(const void *q, const pa_cache_t *cache, int layer, const int32_t *
  * GPU that loads libpa holds that array until the process exits.  This
  * entry point allocates nothing: no cudaMalloc, no cudaFree, no allocating
  * library call.  The first call on a device looks up the array's device
- * address for that device (with that device current) and remembers it;
- * make that first call before any stream capture starts.
+ * address for that device (with that device current) and remembers it
+ * together with the device's current context; make that first call before
+ * any stream capture starts.  A device reset (cudaDeviceReset) re-creates
+ * the context and may move the array: the next call sees the new context
+ * and looks the address up again, so it too must come before any capture.
  *
  * Arguments, results and device-side checks are those of pa_decode.  Each
  * call clears the arrival counters in the array on `stream` before the
  * kernel runs.  All calls in the process share the one array, so two calls
  * that run at the same time on the GPU (on different streams, or from
  * different threads) race and corrupt each other's results: serialise them.
- * Returns PA_ERR_WORKSPACE when num_seqs * n_kv_heads is too large for the
- * array (pa_decode_workspace_bytes(...) > PA_DECODE_NOALLOC_SCRATCH_BYTES).
+ * Returns PA_ERR_WORKSPACE when the call needs more than the array holds
+ * (pa_decode_workspace_bytes(...) > PA_DECODE_NOALLOC_SCRATCH_BYTES).  The
+ * 8 MiB array holds the 608 per-CTA records (608 * 8448 B = 4.9 MiB at
+ * head_dim 128, 2.5 MiB at 64) plus 4 bytes of counter per (sequence, KV
+ * head), i.e. up to about 813 k (sequence, KV head) pairs at head_dim 128.
+ * Up to 195 KV heads the bound that binds first is pa_decode's own
+ * num_seqs <= 4096.
  */
 #define PA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,

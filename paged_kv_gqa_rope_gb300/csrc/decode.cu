@@ -835,21 +835,41 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_
     return counters_bytes(num_seqs, n_kv_heads) + (size_t)kMaxGrid * cta_record_bytes(head_dim);
 }
 
-extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
-                         const int32_t *block_tables, int max_blocks_per_seq,
-                         const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
-                         int head_dim, float scale, void *workspace, size_t workspace_bytes,
-                         void *out, int32_t *dev_status, pa_stream_t stream) {
+namespace pa {
+namespace {
+
+// The argument checks of pa_decode that do not involve the workspace, in
+// the order pa_decode makes them.  PA_OK with num_seqs == 0 means "nothing
+// to do".
+int check_decode_args(const void *q, const pa_cache_t *cache, int layer,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                      int head_dim, float scale, const void *out) {
     if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
-        max_blocks_per_seq <= 0 || !(scale >= 0.f))
+        max_blocks_per_seq <= 0 || max_blocks_per_seq > kMaxBlocksPerSeq || !(scale >= 0.f))
         return PA_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (n_heads / n_kv_heads > kGroupPad || num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
     if (!cache_ok(cache, layer, n_kv_heads, head_dim)) return PA_ERR_INVALID;
     if (num_seqs == 0) return PA_OK;
-    if (!q || !block_tables || !context_lens || !out || !workspace) return PA_ERR_INVALID;
-    if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return PA_ERR_INVALID;
+    if (!q || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(out)) return PA_ERR_INVALID;
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode(const void *q, const pa_cache_t *cache, int layer,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int n_heads, int n_kv_heads,
+                         int head_dim, float scale, void *workspace, size_t workspace_bytes,
+                         void *out, int32_t *dev_status, pa_stream_t stream) {
+    const int rc = check_decode_args(q, cache, layer, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, n_heads, n_kv_heads, head_dim, scale,
+                                     out);
+    if (rc != PA_OK || num_seqs == 0) return rc;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_INVALID;
     const size_t cnt = counters_bytes(num_seqs, n_kv_heads);
     if (workspace_bytes < cnt + cta_record_bytes(head_dim)) return PA_ERR_WORKSPACE;
     // A smaller workspace only narrows the grid.
@@ -934,7 +954,7 @@ extern "C" int pa_decode_i8(const void *q, const pa_cache_i8_t *cache, int layer
                             size_t workspace_bytes, void *out, int32_t *dev_status,
                             pa_stream_t stream) {
     if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
-        max_blocks_per_seq <= 0 || !(scale >= 0.f))
+        max_blocks_per_seq <= 0 || max_blocks_per_seq > kMaxBlocksPerSeq || !(scale >= 0.f))
         return PA_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (n_heads / n_kv_heads > kGroupPad || num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
@@ -990,8 +1010,33 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[PA_DECODE_NOALLOC_SCR
 namespace pa {
 namespace {
 
+// cuCtxGetCurrent, obtained from the driver at run time like
+// cuTensorMapEncodeTiled (the library does not link libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Per device: the context the array's address was looked up in, and the
+// address.  A device reset (or any re-creation of the primary context)
+// loads the module again, possibly at another address; the context handle
+// then differs and the address is looked up again.
+struct NoallocSlot {
+    CUcontext ctx = nullptr;
+    void *ptr = nullptr;
+};
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {nullptr};
+NoallocSlot g_noalloc[64];
 
 int noalloc_scratch(void **out) {
     int dev = 0;
@@ -999,16 +1044,24 @@ int noalloc_scratch(void **out) {
         cudaGetLastError();
         return PA_ERR_CUDA;
     }
+    // The current context may not exist yet on the first call: the symbol
+    // lookup below creates it, and the context is read again after it.
+    CtxGetCurrentFn get_ctx = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (get_ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocSlot &slot = g_noalloc[dev];
+    if (!slot.ptr || !ctx || slot.ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return PA_ERR_CUDA;
         }
-        g_noalloc_ptr[dev] = p;
+        if (!ctx && get_ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+        slot.ptr = p;
+        slot.ctx = ctx;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = slot.ptr;
     return PA_OK;
 }
 
@@ -1020,14 +1073,19 @@ extern "C" int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int lay
                                  const int32_t *context_lens, int num_seqs, int n_heads,
                                  int n_kv_heads, int head_dim, float scale, void *out,
                                  int32_t *dev_status, pa_stream_t stream) {
-    if (num_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return PA_ERR_INVALID;
-    if (num_seqs == 0) return PA_OK;
+    // The same checks, in the same order, as pa_decode, before anything is
+    // enqueued: the two entry points return the same codes for the same
+    // arguments.
+    const int rc = check_decode_args(q, cache, layer, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, n_heads, n_kv_heads, head_dim, scale,
+                                     out);
+    if (rc != PA_OK || num_seqs == 0) return rc;
     const size_t need = pa_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim);
     if (need == 0) return PA_ERR_INVALID;
     if (need > PA_DECODE_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
     void *scratch = nullptr;
-    const int rc = noalloc_scratch(&scratch);
-    if (rc != PA_OK) return rc;
+    const int src = noalloc_scratch(&scratch);
+    if (src != PA_OK) return src;
     // Counters must start at zero; an earlier call that stopped early may
     // have left some behind.
     if (cudaMemsetAsync(scratch, 0, counters_bytes(num_seqs, n_kv_heads),

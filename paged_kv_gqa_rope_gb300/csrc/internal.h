@@ -15,6 +15,10 @@ namespace pa {
 // Tokens per cache block the kernels are built for.
 constexpr int kBlockSize = 16;
 
+// Widest block table the kernels accept: a sequence's length bound
+// max_blocks_per_seq * kBlockSize must fit in int32.
+constexpr int kMaxBlocksPerSeq = INT32_MAX / kBlockSize;
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool cache_ok(const pa_cache_t *c, int layer, int n_kv_heads, int head_dim) {

@@ -974,7 +974,8 @@ extern "C" int pa_prefill_varlen(const void *q, int total_q, const pa_cache_t *c
                                  int head_dim, float scale, void *out, int32_t *dev_status,
                                  pa_stream_t stream) {
     if (n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 || num_seqs < 0 ||
-        total_q < 0 || max_seqlen_q < 0 || max_blocks_per_seq <= 0 || !(scale >= 0.f))
+        total_q < 0 || max_seqlen_q < 0 || max_blocks_per_seq <= 0 ||
+        max_blocks_per_seq > kMaxBlocksPerSeq || !(scale >= 0.f))
         return PA_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;

@@ -273,3 +273,63 @@ def test_prepare_metadata_random_batches_match_oracle(libpa):
         want = orc.decode_metadata(dec, table, bs)
         for key in ("positions", "slot_mapping", "context_lens"):
             assert np.array_equal(got[key], want[key]), (trial, key)
+
+
+def test_c_entry_points_bound_the_block_table_width(libpa):
+    """max_blocks_per_seq * 16 must fit in int32 (the kernels' length bound):
+    every attention entry point refuses a wider table through the C ABI, not
+    only the Python binding."""
+    d = pa.PaCache()
+    fake = ctypes.c_void_p(1 << 20)
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 2, 64, fake) == pa.PA_OK
+    buf = ctypes.c_void_p(1 << 24)
+    widest = (2**31 - 1) // 16
+    for maxb, want in ((widest + 1, pa.PA_ERR_INVALID), (2**31 - 1, pa.PA_ERR_INVALID)):
+        assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, maxb, buf, 2, 4, 2, 64, 0.0, buf,
+                               1 << 24, buf, None, None) == want
+        assert libpa.pa_decode_noalloc(buf, ctypes.byref(d), 0, buf, maxb, buf, 2, 4, 2, 64,
+                                       0.0, buf, None, None) == want
+        assert libpa.pa_prefill_varlen(buf, 8, ctypes.byref(d), 0, buf, buf, buf, maxb, 2, 16, 4,
+                                       2, 64, 0.0, buf, None, None) == want
+        assert libpa.pa_decode_i8(buf, None, 0, buf, maxb, buf, 2, 4, 2, 64, 0.0, buf, 1 << 24,
+                                  buf, None, None) == want
+    # the widest accepted table passes this check (and stops at the next one:
+    # a workspace of 16 bytes is too small)
+    assert libpa.pa_decode(buf, ctypes.byref(d), 0, buf, widest, buf, 2, 4, 2, 64, 0.0, buf, 16,
+                           buf, None, None) == pa.PA_ERR_WORKSPACE
+
+
+def test_decode_noalloc_checks_arguments_like_decode(libpa):
+    """pa_decode_noalloc makes pa_decode's argument checks, in the same order
+    and before it touches its array: the same arguments give the same codes,
+    num_seqs == 0 included (a no-op only once the cache descriptor and the
+    shape are valid)."""
+    d = pa.PaCache()
+    fake = ctypes.c_void_p(1 << 20)
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 2, 64, fake) == pa.PA_OK
+    buf = ctypes.c_void_p(1 << 24)
+    odd = ctypes.c_void_p((1 << 24) + 8)
+    bad = pa.PaCache()  # all zero: no base pointer
+    cases = [
+        # (q, cache, layer, maxb, B, H, Hk, D, scale, out)
+        (buf, d, 0, 4, 2, 32, 2, 64, 0.0, buf),      # group of 16: unsupported
+        (buf, d, 0, 4, 2, 5, 2, 64, 0.0, buf),       # H % Hk != 0
+        (buf, d, 0, 4, 2, 4, 2, 96, 0.0, buf),       # head_dim 96
+        (buf, d, 0, 4, 5000, 4, 2, 64, 0.0, buf),    # more than 4096 sequences
+        (buf, d, 1, 4, 2, 4, 2, 64, 0.0, buf),       # layer out of range
+        (buf, bad, 0, 4, 2, 4, 2, 64, 0.0, buf),     # no cache
+        (buf, bad, 0, 4, 0, 4, 2, 64, 0.0, buf),     # no cache, no sequences
+        (buf, d, 0, 4, 0, 4, 2, 64, 0.0, buf),       # no sequences: no-op
+        (buf, d, 0, 0, 2, 4, 2, 64, 0.0, buf),       # empty table
+        (buf, d, 0, 4, 2, 4, 2, 64, -1.0, buf),      # negative scale
+        (None, d, 0, 4, 2, 4, 2, 64, 0.0, buf),      # no q
+        (odd, d, 0, 4, 2, 4, 2, 64, 0.0, buf),       # q not 16-byte aligned
+        (buf, d, 0, 4, 2, 4, 2, 64, 0.0, odd),       # out not 16-byte aligned
+    ]
+    for q, c, layer, maxb, B, H, Hk, D, scale, out in cases:
+        want = libpa.pa_decode(q, ctypes.byref(c), layer, buf, maxb, buf, B, H, Hk, D, scale, buf,
+                               1 << 24, out, None, None)
+        got = libpa.pa_decode_noalloc(q, ctypes.byref(c), layer, buf, maxb, buf, B, H, Hk, D,
+                                      scale, out, None, None)
+        assert want != pa.PA_ERR_WORKSPACE
+        assert got == want, (q, layer, maxb, B, H, Hk, D, scale, out, got, want)

@@ -1,9 +1,10 @@
 """pa_decode_noalloc: decode for callers that cannot give the library any
 device memory (a plugin whose host framework owns all device allocations, a
 caller that must not call cudaMalloc while running).  Its scratch lives in a
-fixed array inside libpa.  Called here through the C ABI and compared with
-pa_decode on the same inputs, twice in a row (the second call must not be
-disturbed by what the first left in the shared array).
+fixed array inside libpa.  Called here through the C ABI twice in a row (the
+second call must not be disturbed by what the first left in the shared
+array); each result must be bit for bit pa_decode's (the same kernel on the
+same inputs) and within the attention tolerance of the fp64 oracle.
 
 The file name makes pytest collect it last."""
 
@@ -15,7 +16,7 @@ import torch
 
 from paged_kv_gqa_rope_gb300 import pa
 from paged_kv_gqa_rope_gb300 import workloads as W
-from tests.gpu_helpers import DecodeRun, assert_attention_close
+from tests.gpu_helpers import DecodeRun, assert_attention_close, oracle_decode_step
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +57,8 @@ def test_decode_noalloc_matches_decode(libpa):
     run = DecodeRun(case, init)
     ref = run.run()                      # RoPE + append + pa_decode (caller workspace)
     assert int(run.status.item()) == 0
+    _, _, _, want = oracle_decode_step(case, init)
+    assert_attention_close(ref, want)
     for _ in range(2):
         out = torch.full_like(ref, float("nan"))
         status = pa.new_status()
@@ -63,17 +66,20 @@ def test_decode_noalloc_matches_decode(libpa):
         assert rc == pa.PA_OK, pa.strerror(rc)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert_attention_close(out, ref.double().cpu().numpy())
+        assert torch.equal(out, ref)     # same kernel, same inputs: same bits
+        assert_attention_close(out, want)
 
 
 def test_decode_noalloc_rejects_too_large(libpa):
-    case, init = _case(32)
-    run = DecodeRun(case, init)
-    wl = case.wl
-    too_many = 4096
-    assert pa.decode_workspace_bytes(too_many, 512, 256, 128) > (8 << 20)
-    rc = libpa.pa_decode_noalloc(
-        ctypes.c_void_p(run.q.data_ptr()), ctypes.byref(run.cache.desc), 0,
-        ctypes.c_void_p(run.bt.data_ptr()), run.bt.shape[1], ctypes.c_void_p(run.ctx.data_ptr()),
-        too_many, 512, 256, wl.head_dim, 0.0, ctypes.c_void_p(run.q.data_ptr()), None, None)
+    """4096 sequences x 256 KV heads need 4 MiB of counters on top of the
+    4.9 MiB of records: more than the 8 MiB array.  Refused before anything
+    is enqueued (the descriptor wraps an address that is never touched)."""
+    d = pa.PaCache()
+    fake = ctypes.c_void_p(1 << 20)
+    assert libpa.pa_alloc_cache(ctypes.byref(d), 1, 10, 16, 256, 128, fake) == pa.PA_OK
+    buf = ctypes.c_void_p(1 << 24)
+    assert pa.decode_workspace_bytes(4096, 512, 256, 128) > (8 << 20)
+    assert pa.decode_workspace_bytes(4096, 512, 195, 128) <= (8 << 20)
+    rc = libpa.pa_decode_noalloc(buf, ctypes.byref(d), 0, buf, 4, buf, 4096, 512, 256, 128, 0.0,
+                                 buf, None, None)
     assert rc == pa.PA_ERR_WORKSPACE
