@@ -193,8 +193,8 @@ int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *positions,
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
  *                (max_blocks_per_seq * 16 must stay within INT32_MAX: the
  *                kernel bounds L_k by it in int32)
- *   max_seqlen_q host bound on any L_q (sizes the grid; longer sequences
- *                set PA_DEV_BAD_LENGTH and are not computed past it)
+ *   max_seqlen_q host bound on any L_q (a longer sequence sets
+ *                PA_DEV_BAD_LENGTH; its rows are still computed)
  *   out          device fp16 [total_q][n_heads][head_dim]
  *   scale        softmax scale; pass 0 for 1/sqrt(head_dim)
  * Built for head_dim 64 and 128, any n_heads divisible by n_kv_heads and

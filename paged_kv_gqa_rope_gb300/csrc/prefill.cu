@@ -7,10 +7,13 @@
 // stream and block_tables locate every key, prefix and new, in the cache).
 //
 // Work unit: 256 query rows (two 128-row tiles) of one sequence and one Q
-// head.  Row i of a sequence with a cached prefix of p keys sits at
-// absolute position p + i and sees keys 0 .. p + i; key tiles of 128 keys
-// (8 cache blocks) past a tile's last row are never loaded, and only the
-// tiles that reach past a tile's first row are masked.
+// head; both tiles read the same K/V tiles, so each K/V byte brought to the
+// SM serves 256 rows (a paged K/V tile takes a few microseconds to arrive,
+// and the rings that hide that fit in shared memory only at this rate).
+// Row i of a sequence with a cached prefix of p keys sits at absolute
+// position p + i and sees keys 0 .. p + i; key tiles of 128 keys (8 cache
+// blocks) past a tile's last row are never loaded, and only the tiles that
+// reach past a tile's first row are masked.
 //
 // Schedule: units are ordered (sequence, head, row pair from the last to the
 // first) and handed out in that order by a global work counter to the CTAs
@@ -18,38 +21,38 @@
 // work on neighbouring units, mostly of the same heads, and read each K/V
 // tile from L2 rather than each from HBM; the sequences are listed from the
 // costliest to the cheapest and within a head the costliest pair goes first,
-// so the cheap units close the list, which evens out the CTAs' ends.
+// so the cheap units close the list, which evens out the CTAs' ends.  When
+// the scheduler takes a unit it asks L2 for the unit's Q tiles, so their
+// later load into shared memory is an L2 hit.
 //
-// Roles (512 threads):
-//   warps 0-3   softmax of query tile 0 (thread i owns row i = TMEM lane i)
-//   warps 4-7   softmax of query tile 1
-//   warp 8      producer of the two Q tiles and the K tiles, warp 10 of the
-//               V tiles: TMA loads of one 16-token block x 64-column half
-//               at a time, gathered through the block table into rings (K:
-//               2 stages, V: 3 when shared memory allows, else 2), each
-//               refilled as soon as its own slot is free
-//   warp 9      MMA issuer (one thread) and TMEM owner
-//   warp 11     scheduler: takes the CTA's next units from the launch's
-//               work counter into a ring in shared memory
-//   warps 12-15 output: O_t / l of a finished tile to global memory, while
-//               the softmax warpgroups already work on the next unit
-// Tensor memory (512 columns): S0 | S1 | O0 | O1 (128 columns per score
-// tile, head_dim per O).  Per key tile j the MMA thread issues, in order,
-//   O0 += P0 . V_j   (A = P0 from TMEM, once softmax_0 wrote it over S0)
-//   S0  = Q0 . K_j+1^T (same TMEM as P0: tcgen05.mma operations issued by
-//                       one thread execute in issue order, so the P.V has
-//                       read P0 before S0 is written; no wait in between)
-//   O1 += P1 . V_j,  S1 = Q1 . K_j+1^T
-// so softmax_0 works on S0(j+1) while the tensor core runs tile 1's MMAs and
-// softmax_1 while it runs tile 0's.  Each P_t.V_j runs in two halves of 64
-// keys: the first as soon as the softmax has written P for them, the second
-// once the whole tile's P is written.  Every MMA has N = 128 (M = 128,
-// K = 16): a tcgen05.mma takes about 96 cycles at any N up to 128, so wide
-// tiles use the tensor core better.  The running maximum only moves when a
-// half tile raises it by more than 8 (log2 units), so P <= 256 and O is
-// rescaled (in TMEM) only then.  The row sum adds P in fp32 before its
-// rounding to fp16 (the two differ by far less than the output's own fp16
-// rounding).
+// Pipeline.  Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, the score
+// tile of each query tile (128 keys) and its output accumulator.  Per key
+// tile the softmax of tile t reads S_t in two 64-column halves and writes
+// each half's P as fp16 over S_t's first columns, handing the first half to
+// the tensor core at once; O_t += P.V runs in the same two halves, and the
+// next key tile's S_t goes into the same TMEM after it.  Each query tile has
+// its own MMA thread, so one tile's softmax runs while the tensor core works
+// on the other's P.V and next scores, and neither tile's MMAs wait behind the
+// other's synchronisation.
+//
+// Roles (512 threads, 128 registers each):
+//   warps 0-3, 4-7   softmax of query tile 0 / 1 (thread i owns row i =
+//                    TMEM lane i): running maximum and sum, P = 2^(s * scale
+//                    * log2 e - m) in fp16
+//   warp 8           producer of the Q tiles and the K tiles, and scheduler:
+//                    takes the CTA's next unit from the launch's work counter
+//                    into a ring in shared memory; warp 10 producer of the V
+//                    tiles: TMA loads of one 16-token block x 64-column half
+//                    at a time, gathered through the block table into rings
+//                    (K: 3 stages, V: 2 at head_dim 128)
+//   warps 9, 11      MMA issuers of query tile 0 / 1 (one thread each);
+//                    warp 9 owns the TMEM
+//   warps 12-15      output: O_t / l of a finished tile to global memory,
+//                    while the softmax warpgroups work on the next unit
+// The running maximum only moves when a half tile raises it by more than 8
+// (log2 units), so P <= 256 and O is rescaled (in TMEM) only then.  The row
+// sum adds P in fp32 before its rounding to fp16 (the two differ by far
+// less than the output's own fp16 rounding).
 //
 // Bound: tensor cores.  Algorithmic FLOPs = 4 * d * H * (number of visible
 // (query, key) pairs).
@@ -64,23 +67,21 @@
 namespace pa {
 namespace {
 
-constexpr int kBM = 128;  // query rows per tile
-constexpr int kBN = 128;  // keys per tile
+constexpr int kBM = 128;   // query rows per tile
+constexpr int kBN = 128;   // keys per K/V tile
 constexpr int kBlocksPerTile = kBN / kBlockSize;
 constexpr int kUnitRows = 2 * kBM;
-constexpr int kKStages = 2;  // K ring; the V ring has VS = 2 or 3 stages
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kProducerWarp = 8;   // also the scheduler
+constexpr int kMmaWarp = 9;        // query tile 0; warp 11 issues tile 1's
 constexpr int kVProducerWarp = 10;
+constexpr int kMma1Warp = 11;
 constexpr int kEpilogueWarp = 12;  // warps 12-15
-constexpr int kThreads = 16 * 32;  // 128 registers per thread, no spills
+constexpr int kThreads = 16 * 32;  // 128 registers per thread
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSeqs = 2048;
-constexpr int kSchedWarp = 11;
 constexpr int kRing = 8;             // scheduled units buffered per CTA
 constexpr int kRingConsumers = 15;   // warps that read every ring entry
-constexpr int kRingByte = 512;       // offset of the ring (kRing x 32 bytes) in the barrier area
 constexpr int kSchedSlots = 64;      // launches that may run at the same time
 
 // Work counters of the dynamic unit schedule, one pair per launch slot: the
@@ -100,48 +101,61 @@ struct PrefillArgs {
     int sched;  // launch slot of the work counters
 };
 
-template <int D, int VS>
+// Shared memory: a small area of barriers, the unit ring, row sums and the
+// sequence table at the start of the window (16-byte aligned), then, from
+// the next 1024-byte boundary (128-byte swizzle), the operand tiles.
+constexpr int kRingOff = 448;                    // barriers + TMEM slot before it
+constexpr int kLsumOff = kRingOff + kRing * 32;  // float [2 tiles][128]: row sums
+constexpr int kTabOff = kLsumOff + 2 * 128 * 4;  // int4 [B + 1]: sequence table
+// int [B] after the table: sequence of each table row (ranked batches)
+__host__ __device__ __forceinline__ int misc_bytes(int B, bool ranked) {
+    return (kTabOff + (B + 1) * 16 + (ranked ? B * 4 : 0) + 15) & ~15;
+}
+
+template <int D, int KS, int VS>
 struct PL {
     static constexpr int kQHalf = kBM * 128;          // one 64-column half of a Q tile
     static constexpr int kQTile = kQHalf * (D / 64);
     static constexpr int kKVHalf = kBN * 128;         // one 64-column half of a K/V tile
     static constexpr int kKVTile = kKVHalf * (D / 64);
     static constexpr int kQ = 0;                      // 2 query tiles
-    static constexpr int kK = 2 * kQTile;             // kKStages stages
-    static constexpr int kV = kK + kKStages * kKVTile;  // VS stages
-    static constexpr int kBar = kV + VS * kKVTile;
-    static constexpr int kLsum = kBar + 1024;         // float [2 tiles][2 units][128]: row sums
-    static constexpr int kSeqId = kLsum + 2048;       // int [kThreads]: sequence of each table row
-    static constexpr int kTab = kSeqId + 4 * kThreads;  // int4 [B + 1]: sequence table
-    static size_t bytes(int B) { return (size_t)kTab + (size_t)(B + 1) * 16; }
-    static constexpr int kOCol = 2 * kBN;             // O_t at kOCol + t * D
+    static constexpr int kK = 2 * kQTile;             // KS stages
+    static constexpr int kV = kK + KS * kKVTile;      // VS stages
+    static constexpr int kTiles = kV + VS * kKVTile;
+    // The window: the small area, at most 1008 bytes to the 1024-byte
+    // boundary (the window starts 16-byte aligned), the tiles.
+    static size_t bytes(int B, bool ranked) {
+        return (size_t)misc_bytes(B, ranked) + 1008 + (size_t)kTiles;
+    }
 };
 
-// TMEM column of the score tile of query tile t.
+// TMEM columns: the score tile of query tile t at t * 128 (its P over the
+// first 64 columns), O_t at 256 + t * D.
 __device__ __forceinline__ uint32_t s_col(int t) { return (uint32_t)(t * kBN); }
+__device__ __forceinline__ uint32_t o_col(int t, int D) { return (uint32_t)(2 * kBN + t * D); }
 
 enum {
     B_QFULL = 0,    // per query tile
     B_QEMPTY = 2,   // per query tile
-    B_KFULL = 4,    // kKStages
-    B_KEMPTY = 6,   // kKStages
-    B_VFULL = 8,    // up to 3 V stages
-    B_VEMPTY = 11,  // up to 3
-    B_VFIXED = 14,  // up to 3: a V tile whose tail rows were cleared
-    B_SFULL = 17,   // per query tile
-    B_PREADY = 19,  // per query tile
-    B_ODONE = 21,   // per query tile
-    B_OFREE = 23,   // per query tile
-    B_DRAIN = 25,
-    B_LREADY = 26,  // per query tile and unit parity: row sums written
-    B_UFULL = 30,   // kRing: unit ring entry written
-    B_UEMPTY = 38,  // kRing: entry read by every consumer warp
-    B_KSTART = 46,  // the K producer started a unit
-    B_PHALF = 47,   // per query tile: P of the score tile's first 64 keys written
-    B_OHALF = 49,   // per query tile: the P.V of those 64 keys done
-    B_COUNT = 51
+    B_KFULL = 4,    // up to 3 K stages
+    B_KEMPTY = 7,   // up to 3
+    B_VFULL = 10,   // up to 3 V stages
+    B_VEMPTY = 13,  // up to 3
+    B_VFIXED = 16,  // up to 3: a V tile whose tail rows were cleared
+    B_SFULL = 19,   // per query tile: scores written
+    B_PHALF = 21,   // per query tile: P of the first 64 keys written
+    B_PREADY = 23,  // per query tile: P of all 128 keys written
+    B_OHALF = 25,   // per query tile: the P.V of the first 64 keys done
+    B_OUNIT = 29,   // per query tile: the unit's last P.V done
+    B_OFREE = 31,   // per query tile: O_t read out
+    B_LREADY = 33,  // per query tile: row sums of a unit written
+    B_LFREE = 35,   // per query tile: row sums read
+    B_DRAIN = 37,   // per query tile
+    B_UFULL = 39,   // kRing: unit ring entry written
+    B_UEMPTY = 47,  // kRing: entry read by every consumer warp
+    B_COUNT = 55
 };
-static_assert(B_COUNT * 8 + 4 <= kRingByte && kRingByte + kRing * 32 <= 1024, "barrier area");
+static_assert(B_COUNT * 8 + 4 <= kRingOff, "barrier area");
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2, int c3) {
@@ -150,6 +164,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
         "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Prefetch one 4-D box into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                int c3) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 
@@ -294,6 +318,13 @@ struct UnitIter {
         ps = pair_shape(p, si.L_q, k);
     }
     __device__ __forceinline__ bool valid(int total) const { return u < total; }
+    __device__ __forceinline__ int nmax() const { return max(ps.n[0], ps.n[1]); }
+    // The last K/V tile holds the sequence's last block, which ends inside
+    // the block: its V rows past k_len are cleared before P.V reads them.
+    __device__ __forceinline__ bool fix_tail() const {
+        const int nblk_k = (si.k_len + kBlockSize - 1) / kBlockSize;
+        return (si.k_len % kBlockSize) != 0 && (nblk_k - 1) / kBlocksPerTile == nmax() - 1;
+    }
 };
 
 // A CTA that has taken its last unit; the last such CTA of the launch clears
@@ -306,20 +337,21 @@ __device__ __forceinline__ void sched_finish(int slot) {
     }
 }
 
-template <int D, int VS>
+template <int D, int KS, int VS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kvmap, const PrefillArgs a) {
-    using L = PL<D, VS>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
-    int4 *tab = reinterpret_cast<int4 *>(smem + L::kTab);
-
+    using L = PL<D, KS, VS>;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
+    const bool ranked = B <= kThreads;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+    int4 *tab = reinterpret_cast<int4 *>(smem_raw + kTabOff);
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + misc_bytes(B, ranked) + 1023) &
+        ~static_cast<uintptr_t>(1023));
 
     // ---- sequence table: lengths and the running count of units
     for (int s = tid; s < B; s += kThreads) {
@@ -340,8 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     // ---- sequences from the costliest (visible query-key pairs) to the
     // cheapest: rank by counting, one sequence per thread
-    int *seqid = reinterpret_cast<int *>(smem + L::kSeqId);
-    const bool ranked = B <= kThreads;
+    int *seqid = reinterpret_cast<int *>(tab + B + 1);
     if (ranked) {
         int4 mine = make_int4(0, 0, 0, 0);
         int rank = 0;
@@ -381,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    // ---- unit ring: entry 0 taken here, the rest by the scheduler warp
-    int4 *uring = reinterpret_cast<int4 *>(smem + L::kBar + kRingByte);  // 2 x int4 per entry
+    // ---- unit ring: entry 0 taken here, the rest by the K producer warp
+    int4 *uring = reinterpret_cast<int4 *>(smem_raw + kRingOff);  // 2 x int4 per entry
     const int total_units = tab[B].x;
     if (tid == 0) {
         UnitIter u0;
@@ -397,33 +428,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < kKStages; ++i) {
+        // a K or V stage is free once both MMA threads are done with it
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&bar[B_KFULL + i], 1);
-            mbar_init(&bar[B_KEMPTY + i], 1);
+            mbar_init(&bar[B_KEMPTY + i], 2);
         }
         for (int i = 0; i < VS; ++i) {
             mbar_init(&bar[B_VFULL + i], 1);
-            mbar_init(&bar[B_VEMPTY + i], 1);
+            mbar_init(&bar[B_VEMPTY + i], 2);
             mbar_init(&bar[B_VFIXED + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar[B_QFULL + i], 1);
             mbar_init(&bar[B_QEMPTY + i], 1);
             mbar_init(&bar[B_SFULL + i], 1);
-            mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_PHALF + i], 128);
+            mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_OHALF + i], 1);
-            mbar_init(&bar[B_ODONE + i], 1);
+            mbar_init(&bar[B_OUNIT + i], 1);
             mbar_init(&bar[B_OFREE + i], 128);
-            mbar_init(&bar[B_LREADY + 2 * i], 128);
-            mbar_init(&bar[B_LREADY + 2 * i + 1], 128);
+            mbar_init(&bar[B_LREADY + i], 128);
+            mbar_init(&bar[B_LFREE + i], 128);
         }
         mbar_init(&bar[B_DRAIN], 1);
+        mbar_init(&bar[B_DRAIN + 1], 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&bar[B_UFULL + i], 1);
             mbar_init(&bar[B_UEMPTY + i], kRingConsumers);
         }
-        mbar_init(&bar[B_KSTART], 1);
         fence_barrier_init();
         mbar_arrive(&bar[B_UFULL]);  // entry 0 is in place
     }
@@ -440,22 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const int oob_row = a.num_blocks * kBlockSize;  // zero-filled by TMA
 
-    float *lsum = reinterpret_cast<float *>(smem + L::kLsum);
-    // Unit of ring entry i, for one thread of a consumer warp (the MMA
-    // issuer): waits for the entry and releases it (one arrival per warp).
-    auto take0 = [&](int i) -> UnitIter {
-        const int slot = i % kRing;
-        UnitIter u;
-        u.u = INT_MAX;
-        if (!mbar_wait(&bar[B_UFULL + slot], (i / kRing) & 1)) {
-            report(a.status, PA_DEV_TIMEOUT);
-            return u;
-        }
-        u.load(uring + 2 * slot);
-        mbar_arrive(&bar[B_UEMPTY + slot]);
-        return u;
-    };
-    // The same for a whole warp: every lane waits and reads, lane 0 releases.
+    float *lsum = reinterpret_cast<float *>(smem_raw + kLsumOff);
+    // Unit of ring entry i for a whole warp: every lane waits and reads,
+    // lane 0 releases the entry (one arrival per warp).
     auto take = [&](int i) -> UnitIter {
         const int slot = i % kRing;
         UnitIter u;
@@ -472,31 +491,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         return u;
     };
 
+    // The same for one thread of a consumer warp (the MMA issuer).
+    auto take0 = [&](int i) -> UnitIter {
+        const int slot = i % kRing;
+        UnitIter u;
+        u.u = INT_MAX;
+        if (!mbar_wait(&bar[B_UFULL + slot], (i / kRing) & 1)) {
+            report(a.status, PA_DEV_TIMEOUT);
+            return u;
+        }
+        u.load(uring + 2 * slot);
+        mbar_arrive(&bar[B_UEMPTY + slot]);
+        return u;
+    };
+
     if (warp >= kEpilogueWarp) {
         // ======================= output warpgroup: thread = query row of the
-        // finished tile.  It reads O_t once the unit's last P.V completed,
-        // releases O_t to the next unit and stores O_t / l; the softmax
-        // warpgroups meanwhile work on the next unit.
+        // finished tile.  It reads O_t once the unit's last P.V of the tile
+        // completed, releases O_t to the next unit and stores O_t / l; the
+        // softmax warpgroups meanwhile work on the next unit.
         const int r = tid - kEpilogueWarp * 32;  // TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        int g0 = 0, g1 = 0;    // score tiles of query tile 0 / 1 in earlier units
         int un0 = 0, un1 = 0;  // earlier units with rows in query tile 0 / 1
         int ui = 0;            // ring entry
         for (UnitIter u = take(0); u.valid(total_units) && ok; u = take(++ui)) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                const int n = u.ps.tiles(t);
-                int &g = t ? g1 : g0;
                 int &un = t ? un1 : un0;
-                if (!ok || n == 0) continue;
-                const int slot = 2 * t + (un & 1);
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bar[B_LREADY + slot], (un >> 1) & 1) &&
-                                    mbar_wait(&bar[B_ODONE + t], (g + n - 1) & 1));
+                if (!ok || u.ps.tiles(t) == 0) continue;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_LREADY + t], un & 1) &&
+                                                 mbar_wait(&bar[B_OUNIT + t], un & 1));
                 if (!ok) continue;
                 tc::fence_after();
-                const float l = lsum[slot * 128 + r];
+                const float l = lsum[t * 128 + r];
+                mbar_arrive(&bar[B_LFREE + t]);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const bool row_valid = r < u.ps.rows(t);
                 uint4 *dst = reinterpret_cast<uint4 *>(
@@ -506,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
-                    tc::ld32(tmem + lane_base + L::kOCol + t * D + c * 32, orr);
+                    tc::ld32(tmem + lane_base + o_col(t, D) + c * 32, orr);
                     if (c == D / 32 - 1) {
                         tc::fence_before();
                         mbar_arrive(&bar[B_OFREE + t]);  // the next unit may overwrite O_t
@@ -521,7 +550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[c * 4 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
                     }
                 }
-                g += n;
                 ++un;
             }
         }
@@ -533,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool is_v = warp == kVProducerWarp;
         const int full0 = is_v ? B_VFULL : B_KFULL;
         const int empty0 = is_v ? B_VEMPTY : B_KEMPTY;
-        const int nst = is_v ? VS : kKStages;  // ring depth
+        const int nst = is_v ? VS : KS;  // ring depth
         const int plane = is_v ? a.plane_v : a.plane_k;
         uint8_t *const ring = smem + (is_v ? L::kV : L::kK);
         int ok = 1;
@@ -555,25 +583,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int kvc = 0, qn0 = 0, qn1 = 0;  // K/V tiles, Q tiles per query tile, loaded so far
         int ui = 0;                     // ring entry
-        UnitIter u = take(0), un;
+        // The K producer is also the scheduler: as it starts a unit it takes
+        // the CTA's next unit from the launch's work counter into the next
+        // ring entry (one unit ahead hides the counter's latency, and no more
+        // is claimed, so the CTAs' last units end close together), and asks
+        // L2 for that unit's Q tiles.  The ring ends with one entry past the
+        // last unit.
+        auto schedule = [&](int i) -> UnitIter {
+            const int slot = i % kRing;
+            int okw = 1;
+            if (lane == 0) {
+                if (i >= kRing) okw = mbar_wait(&bar[B_UEMPTY + slot], ((i / kRing) - 1) & 1);
+                UnitIter v;
+                v.decode(B, tab, ranked ? seqid : nullptr,
+                         okw ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units)
+                             : total_units);
+                v.store(uring + 2 * slot);
+                mbar_arrive(&bar[B_UFULL + slot]);
+                if (v.u >= total_units) {
+                    sched_finish(a.sched);
+                } else {
+                    const int rows = min(kUnitRows, v.si.L_q - v.k * kUnitRows);
+                    for (int t = 0; t < 2 && t * kBM < rows; ++t)
+                        for (int hf = 0; hf < D / 64; ++hf)
+                            tma_prefetch_4d(&qmap, 0, hf, v.h,
+                                            v.si.q_begin + v.k * kUnitRows + t * kBM);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, okw, 0) && ok;
+            __syncwarp();
+            UnitIter v;
+            v.load(uring + 2 * slot);
+            return v;
+        };
+        UnitIter u, un;
+        if (is_v) {
+            u = take(0);
+        } else {
+            u.load(uring);  // entry 0, written in the set-up
+        }
         int rows_cur = u.valid(total_units) ? block_row(u, 0) : 0;
         while (u.valid(total_units) && ok) {
-            // Starting u lets the scheduler take the unit after it: one unit
-            // ahead is enough to hide the counter's latency, and no more is
-            // claimed, so the CTAs' last units end close together.
-            if (!is_v && lane == 0) mbar_arrive(&bar[B_KSTART]);
-            const int nmax = max(u.ps.n[0], u.ps.n[1]);
+            if (!is_v) un = schedule(ui + 1);
+            const int nmax = u.nmax();
             const int kvh = u.h / a.g;
             const int q0 = u.k * kUnitRows;
-            const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
-            const bool fix_tail = is_v && (u.si.k_len % kBlockSize) != 0 &&
-                                  (nblk_k - 1) / kBlocksPerTile == nmax - 1;
+            const bool fix_tail = is_v && u.fix_tail();
             for (int j = 0; j < nmax && ok; ++j) {
                 int rows_next;
                 if (j + 1 < nmax) {
                     rows_next = block_row(u, j + 1);
                 } else {  // the next unit: its first block rows are looked up early
-                    un = take(++ui);
+                    if (is_v) un = take(ui + 1);
                     rows_next = un.valid(total_units) ? block_row(un, 0) : 0;
                 }
                 const int idx = kvc + j;
@@ -597,7 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!is_v && j == 0 && lane == 0) {
                     // Q tiles after K_0: K_0's stage frees earlier than a Q
-                    // buffer, which waits for its tile's last S of the unit before.
+                    // buffer, which waits for its tile's last scores of the
+                    // unit before.
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         int &qn = t ? qn1 : qn0;
@@ -621,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (ok) {
                         uint8_t *vt = smem + L::kV + st * L::kKVTile;
+                        const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
                         const int b_in = (nblk_k - 1) % kBlocksPerTile;
                         const int r0 = u.si.k_len % kBlockSize;
                         const int nrows = kBlockSize - r0;
@@ -641,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             kvc += nmax;
             u = un;
+            ++ui;
         }
         if (lane == 0) {
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
@@ -650,148 +714,117 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!is_v && qn0 > 0) mbar_wait(&bar[B_QFULL], (qn0 - 1) & 1);
             if (!is_v && qn1 > 0) mbar_wait(&bar[B_QFULL + 1], (qn1 - 1) & 1);
         }
-      } else if (warp == kMmaWarp) {
-        // ======================= MMA issuer (one thread)
+      } else {
+        // ======================= MMA issuers: one thread per query tile (warp 9
+        // tile 0, warp 11 tile 1), so one tile's waits and commits overlap
+        // the other's MMAs (an MMA's issue holds its thread for about its
+        // run time).  Per key tile j of its tile: O_t += P.V over the first
+        // 64 keys as soon as the softmax has written their P, then over the
+        // other 64, then S_t(j + 1) = Q_t.K_(j+1)^T into the same TMEM (the
+        // P.V was issued first by this thread: tcgen05.mma operations issued
+        // by one thread execute in issue order).  Each thread releases every
+        // K and V tile of the unit (a stage is refilled once both have), also
+        // those its tile does not need, after seeing it loaded: so neither
+        // thread can get a ring's depth ahead of the other.
+        const int t = warp == kMma1Warp ? 1 : 0;
         if (lane == 0) {
             constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN, false, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
-            bool ok = true;
-            int kvc = 0;
-            int fixc0 = 0, fixc1 = 0, fixc2 = 0;  // cleared V tiles per V stage
-            int gt[2] = {0, 0};       // score tiles of query tile t in earlier units
-            int units_t[2] = {0, 0};  // earlier units with a non-empty tile t
-            // Shared-memory descriptors of every operand buffer, built once; a
+            // Shared-memory descriptors of the operand buffers, built once; a
             // k-step only adds its byte offset / 16 to the start-address field.
-            const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+            const uint64_t dq = tc::smem_desc_sw128(smem_u32(smem + L::kQ + t * L::kQTile), 16, 1024);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
             const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(smem + L::kV), L::kKVHalf, 1024);
-            // S_t for key tile j of unit u, K from ring stage st.  Its TMEM held
-            // P_t of the previous score tile: the P.V that read it was issued
-            // earlier by this thread, and tcgen05.mma operations issued by one
-            // thread run in issue order.  After the unit's last S_t the Q_t
-            // buffer is released to the next unit.
-            auto issue_s = [&](const UnitIter &u, int t, int j, int st) {
-                const uint64_t dq = dq0 + (uint64_t)((t * L::kQTile) >> 4);
-                const uint64_t dk = dk0 + (uint64_t)((st * L::kKVTile) >> 4);
-                const uint32_t d_tmem = tmem + s_col(t);
+            bool ok = true;
+            int kvc = 0;  // K/V tiles of earlier units
+            int g = 0;    // score tiles of this query tile in earlier units
+            int un = 0;   // earlier units with rows in this tile
+            int fix0 = 0, fix1 = 0, fix2 = 0;  // cleared V tiles per V stage
+            // S_t = Q_t.K^T of K/V tile kvi (K stage kvi % KS).
+            auto issue_s = [&](int kvi) {
+                const uint64_t dk = dk0 + (uint64_t)(((kvi % KS) * L::kKVTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc::mma_ss(d_tmem, dq + (uint64_t)(((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4),
+                    tc::mma_ss(tmem + s_col(t),
+                               dq + (uint64_t)(((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4),
                                dk + (uint64_t)(((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4),
                                kIdescQK, kk > 0);
                 tc::commit(&bar[B_SFULL + t]);
-                if (j + 1 == u.ps.tiles(t)) tc::commit(&bar[B_QEMPTY + t]);
-            };
-            // Both tiles' scores for key tile j of this unit (K from its stage).
-            auto issue_s_tile = [&](const UnitIter &u, int j) -> bool {
-                const int idx = kvc + j;
-                const int st = idx % kKStages;
-                if (!mbar_wait(&bar[B_KFULL + st], (idx / kKStages) & 1)) return false;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= u.ps.tiles(t)) continue;
-                    if (!mbar_wait(&bar[B_QFULL + t], (t ? units_t[1] : units_t[0]) & 1)) return false;
-                    tc::fence_after();
-                    issue_s(u, t, j, st);
-                }
-                tc::commit(&bar[B_KEMPTY + st]);
-                return true;
             };
             int ui = 0;  // ring entry
             for (UnitIter u = take0(0); u.valid(total_units) && ok; u = take0(++ui)) {
-                const int nmax = max(u.ps.n[0], u.ps.n[1]);
-                const int nblk_k = (u.si.k_len + kBlockSize - 1) / kBlockSize;
-                const bool fix_tail = (u.si.k_len % kBlockSize) != 0 &&
-                                      (nblk_k - 1) / kBlocksPerTile == nmax - 1;
-                ok = issue_s_tile(u, 0);
+                const int n = u.ps.tiles(t);
+                const int nmax = u.nmax();
+                const bool fix_tail = u.fix_tail();
+                // ---- K tile 0: the tile's first scores
+                ok = mbar_wait(&bar[B_KFULL + kvc % KS], (kvc / KS) & 1);
+                if (ok && n > 0) ok = mbar_wait(&bar[B_QFULL + t], un & 1);
+                if (!ok) break;
+                tc::fence_after();
+                if (n > 0) {
+                    issue_s(kvc);
+                    if (n == 1) tc::commit(&bar[B_QEMPTY + t]);  // Q_t done
+                }
+                tc::commit(&bar[B_KEMPTY + kvc % KS]);
                 for (int j = 0; j < nmax && ok; ++j) {
-                    const int idx = kvc + j;
-                    const int st = idx % VS;               // V stage of tile j
-                    const int st1 = (idx + 1) % kKStages;  // K stage of tile j+1
-                    // A stage is refilled only after its tile was consumed, so
-                    // per-stage barriers never run two phases ahead.
-                    ok = (fix_tail && j == nmax - 1)
-                             ? mbar_wait(&bar[B_VFIXED + st],
-                                         (st == 0 ? fixc0++ : st == 1 ? fixc1++ : fixc2++) & 1)
-                             : mbar_wait(&bar[B_VFULL + st], (idx / VS) & 1);
-                    tc::fence_after();
-                    const uint64_t dv = dv0 + (uint64_t)((st * L::kKVTile) >> 4);
-                    bool k_next = false;  // K of tile j+1 waited for
-                    // Tile 0's P.V then its next scores, then tile 1's: each
-                    // softmax warpgroup works while the tensor core runs the
-                    // other tile's MMAs.
-                    const int t_last = j < u.ps.n[1] ? 1 : 0;  // last tile to read V_j
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (!ok || j >= u.ps.n[t]) continue;
-                        const int G = gt[t] + j;
-                        // P.V in two halves of 64 keys: the first as soon as
-                        // the softmax has written P for them, the second when
-                        // the whole tile's P is in TMEM.
+                    const int kvi = kvc + j;
+                    const int vs = kvi % VS;
+                    // V tile j (its tail rows cleared first when it holds the
+                    // sequence's last block)
+                    const bool fixed = fix_tail && j == nmax - 1;
+                    ok = fixed ? mbar_wait(&bar[B_VFIXED + vs],
+                                           (vs == 0 ? fix0 : vs == 1 ? fix1 : fix2) & 1)
+                               : mbar_wait(&bar[B_VFULL + vs], (kvi / VS) & 1);
+                    const bool next_k = j + 1 < nmax;
+                    if (ok && next_k)
+                        ok = mbar_wait(&bar[B_KFULL + (kvi + 1) % KS], ((kvi + 1) / KS) & 1);
+                    if (!ok) break;
+                    if (j < n) {
+                        const int G = g + j;  // this score tile
+                        const uint64_t dv = dv0 + (uint64_t)((vs * L::kKVTile) >> 4);
                         ok = mbar_wait(&bar[B_PHALF + t], G & 1);
-                        if (ok && j == 0 && units_t[t] > 0)
-                            ok = mbar_wait(&bar[B_OFREE + t], (units_t[t] - 1) & 1);
+                        // The unit's first P.V overwrites O_t: the output
+                        // warpgroup must have read the previous unit's.
+                        if (ok && j == 0 && un > 0) ok = mbar_wait(&bar[B_OFREE + t], (un - 1) & 1);
+                        if (!ok) break;
                         tc::fence_after();
-                        if (!ok) continue;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 32; ++kk)
-                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t) + kk * 8,
+                            tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kk * 8,
                                        dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
                                        (j > 0 || kk > 0) ? 1u : 0u);
                         tc::commit(&bar[B_OHALF + t]);
                         ok = mbar_wait(&bar[B_PREADY + t], G & 1);
+                        if (!ok) break;
                         tc::fence_after();
-                        if (!ok) continue;
 #pragma unroll
                         for (int kk = kBN / 32; kk < kBN / 16; ++kk)
-                            tc::mma_ts(tmem + L::kOCol + t * D, tmem + s_col(t) + kk * 8,
+                            tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kk * 8,
                                        dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
-                        tc::commit(&bar[B_ODONE + t]);
-                        if (t == t_last) tc::commit(&bar[B_VEMPTY + st]);  // V_j free
-                        if (j + 1 < u.ps.n[t]) {
-                            if (!k_next) {
-                                ok = mbar_wait(&bar[B_KFULL + st1], ((idx + 1) / kKStages) & 1);
-                                tc::fence_after();
-                                k_next = true;
-                            }
-                            if (ok) issue_s(u, t, j + 1, st1);
+                        if (j == n - 1) tc::commit(&bar[B_OUNIT + t]);
+                        if (j + 1 < n) {  // the next scores, over P_t's TMEM
+                            issue_s(kvi + 1);
+                            if (j + 2 == n) tc::commit(&bar[B_QEMPTY + t]);  // Q_t done
                         }
                     }
-                    if (!ok) break;
-                    if (k_next) tc::commit(&bar[B_KEMPTY + st1]);
+                    tc::commit(&bar[B_VEMPTY + vs]);
+                    if (next_k) tc::commit(&bar[B_KEMPTY + (kvi + 1) % KS]);
+                    if (fixed) {
+                        fix0 += vs == 0;
+                        fix1 += vs == 1;
+                        fix2 += vs == 2;
+                    }
                 }
                 kvc += nmax;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    gt[t] += u.ps.n[t];
-                    if (u.ps.n[t] > 0) ++units_t[t];
+                if (n > 0) {
+                    g += n;
+                    ++un;
                 }
             }
             if (!ok) report(a.status, PA_DEV_TIMEOUT);
             // Nothing of ours may still be running when the CTA frees TMEM.
-            tc::commit(&bar[B_DRAIN]);
-            mbar_wait(&bar[B_DRAIN], 0);
-        }
-        __syncwarp();
-      } else if (warp == kSchedWarp) {
-        // ======================= scheduler (one thread): takes the CTA's next
-        // unit from the launch's work counter into the ring once the K
-        // producer started the one before, ending with one past the last unit
-        if (lane == 0) {
-            bool ok = true;
-            for (int i = 1;; ++i) {
-                const int slot = i % kRing;
-                ok = mbar_wait(&bar[B_KSTART], (i - 1) & 1);
-                if (ok && i >= kRing) ok = mbar_wait(&bar[B_UEMPTY + slot], ((i / kRing) - 1) & 1);
-                UnitIter u;
-                u.decode(B, tab, ranked ? seqid : nullptr,
-                         ok ? min(atomicAdd(&g_sched_next[a.sched], 1), total_units) : total_units);
-                u.store(uring + 2 * slot);
-                mbar_arrive(&bar[B_UFULL + slot]);
-                if (u.u >= total_units) break;
-            }
-            if (!ok) report(a.status, PA_DEV_TIMEOUT);
-            sched_finish(a.sched);
+            tc::commit(&bar[B_DRAIN + t]);
+            mbar_wait(&bar[B_DRAIN + t], 0);
         }
         __syncwarp();
       }
@@ -800,12 +833,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp >> 2;      // query tile of this warpgroup
         const int r = tid - t * 128;  // row in the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t o_tmem = tmem + lane_base + L::kOCol + t * D;
+        const uint32_t s_tmem = tmem + lane_base + s_col(t);
+        const uint32_t o_tmem = tmem + lane_base + o_col(t, D);
         const float sl2 = a.scale_log2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         bool ok = true;
         int g = 0;   // score tiles of this query tile in earlier units
         int un = 0;  // earlier units with rows in this query tile
-        const uint32_t s_tmem = tmem + lane_base + s_col(t);
         int ui = 0;  // ring entry
         for (UnitIter u = take(0); u.valid(total_units) && ok; u = take(++ui)) {
             const int n = u.ps.tiles(t);
@@ -813,26 +847,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
             const int key_lim = min(first_row + r, u.si.k_len - 1);
             float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < n; ++j) {
+            for (int j = 0; j < n && ok; ++j) {
                 const int G = g + j;
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], G & 1));
                 if (!ok) break;
                 tc::fence_after();
                 const bool masked = j * kBN + kBN - 1 > first_row;
-                const int kl = key_lim - j * kBN;  // last visible column of this tile
-                const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                // Each 64-column half is read from TMEM once: its maximum, then
-                // P over S; then the half goes to the P.V (keys 0-63 on
-                // B_PHALF, the rest on B_PREADY), so the tensor core starts on
-                // the first half while the second is computed.  A half that
-                // raises the running maximum past the threshold (rare after a
-                // row's first tile) first scales O_t down to it: O_t then holds
-                // the earlier tiles' P.V, and for the second half also this
-                // tile's first-half P.V, made with the old maximum.
+                // Each 64-column half is read from TMEM once with its 32
+                // columns' maxima (tcgen05.ld.red; a masked half takes the
+                // maximum after masking), then its P is written over the
+                // score tile's first columns and handed to the P.V at once
+                // (the first half on B_PHALF, so the tensor core starts on it
+                // while the second is computed).
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
-                    // The TMEM load returns each 32 columns' maximum too
-                    // (tcgen05.ld.red); a masked tile takes it after masking.
                     uint32_t sa[32], sb[32];
                     float ma, mb;
                     tc::ld32_max_issue(s_tmem + hf * 64, sa, ma);
@@ -840,31 +868,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::wait_ld(sa, sb, ma, mb);
                     float mx = fmaxf(ma, mb);
                     if (masked) {
-                        mask_cols(sa, sb, hf * 64, kl);
+                        mask_cols(sa, sb, j * kBN + hf * 64, key_lim);
                         mx = half_max(sa, sb);
                     }
                     const float m_t = mx * sl2;
                     const bool up = m_t > m_used + kRescaleThreshold;
-                    float a = 1.f;
+                    float f = 1.f;
                     if (up) {
-                        a = ex2(m_used - m_t);  // 0 on the first tile
-                        l *= a;
+                        f = ex2(m_used - m_t);  // 0 on the first half
+                        l *= f;
                         m_used = m_t;
                     }
                     if ((j > 0 || hf == 1) && __any_sync(0xffffffffu, up)) {
-                        // O_t must hold the P.V it is scaled with (normally
-                        // complete: the previous tile's was issued before S_t).
-                        ok = __all_sync(0xffffffffu,
-                                        hf == 0 ? mbar_wait(&bar[B_ODONE + t], (G - 1) & 1)
-                                                : mbar_wait(&bar[B_OHALF + t], G & 1));
-                        if (!ok) break;
+                        // O_t holds P.V made with the old maximum: it is scaled
+                        // down to the new one by the whole warp (TMEM loads
+                        // and stores are warp-wide; rows that keep their
+                        // maximum scale by 1).  For the first half that is the
+                        // earlier tiles' P.V, complete: this tile's scores were
+                        // issued after the last of them into the TMEM it read.
+                        // For the second half it also holds this tile's first
+                        // half P.V, waited for here.
+                        if (hf == 1) {
+                            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OHALF + t], G & 1));
+                            if (!ok) break;
+                        }
                         tc::fence_after();
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t orr[32];
                             tc::ld32(o_tmem + c * 32, orr);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * a);
+                            for (int i = 0; i < 32; ++i) orr[i] = f2u(u2f(orr[i]) * f);
                             tc::st32(o_tmem + c * 32, orr);
                         }
                     }
@@ -881,15 +915,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::wait_st();
                     tc::fence_before();
-                    mbar_arrive(&bar[hf == 0 ? B_PHALF + t : B_PREADY + t]);
+                    mbar_arrive(&bar[(hf == 0 ? B_PHALF : B_PREADY) + t]);
                 }
-                if (!ok) break;
             }
             if (!ok) break;
             // The row sum goes to the output warpgroup, which waits for the
-            // unit's last P.V; this warpgroup goes on to the next unit.
-            lsum[(2 * t + (un & 1)) * 128 + r] = l;
-            mbar_arrive(&bar[B_LREADY + 2 * t + (un & 1)]);
+            // unit's last P.V; this warpgroup goes on to the next unit (once
+            // the previous unit's row sum has been read).
+            if (un > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_LFREE + t], (un - 1) & 1));
+                if (!ok) break;
+            }
+            lsum[t * 128 + r] = l;
+            mbar_arrive(&bar[B_LREADY + t]);
             ++un;
             g += n;
         }
@@ -918,17 +956,17 @@ bool make_rows_map(CUtensorMap *map, const void *base, int T, int H, int D) {
 
 constexpr size_t kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per CTA
 
-template <int D, int VS>
+template <int D, int KS, int VS>
 size_t prefill_smem(int B) {
     // At least 116 KB keeps one CTA per SM, so no CTA waits in tcgen05.alloc
     // for another's 512 TMEM columns.
-    const size_t need = PL<D, VS>::bytes(B) + 1024;
+    const size_t need = PL<D, KS, VS>::bytes(B, B <= kThreads);
     return need > 116 * 1024 ? need : 116 * 1024;
 }
 
-template <int D, int VS>
-int launch_prefill_vs(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
-                      cudaStream_t st) {
+template <int D, int KS, int VS>
+int launch_prefill_stages(const CUtensorMap &qmap, const CUtensorMap &kvmap,
+                          const PrefillArgs &a, cudaStream_t st) {
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -936,7 +974,7 @@ int launch_prefill_vs(const CUtensorMap &qmap, const CUtensorMap &kvmap, const P
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(prefill_kernel<D, VS>,
+            if (cudaFuncSetAttribute(prefill_kernel<D, KS, VS>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemLimit) != cudaSuccess) {
                 cudaGetLastError();
@@ -947,19 +985,26 @@ int launch_prefill_vs(const CUtensorMap &qmap, const CUtensorMap &kvmap, const P
     }
     const int grid = sm_count();
     if (grid < 1) return PA_ERR_CUDA;
-    launch_dependent(prefill_kernel<D, VS>, dim3(grid), dim3(kThreads), prefill_smem<D, VS>(a.B),
-                     st, qmap, kvmap, a);
+    launch_dependent(prefill_kernel<D, KS, VS>, dim3(grid), dim3(kThreads),
+                     prefill_smem<D, KS, VS>(a.B), st, qmap, kvmap, a);
     return launch_status();
 }
 
-// Three V stages when the batch's prefix table leaves room for them (they
-// hide the ~3 us a paged V tile takes to arrive); two otherwise.
+// Ring depths at head_dim 128: three K stages and two V stages when the
+// batch's sequence table leaves room for them, two and two otherwise; at
+// head_dim 64 the tiles are half the size and both rings get three.
 template <int D>
 int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
                    cudaStream_t st) {
-    if (prefill_smem<D, 3>(a.B) <= kSmemLimit) return launch_prefill_vs<D, 3>(qmap, kvmap, a, st);
-    if (prefill_smem<D, 2>(a.B) <= kSmemLimit) return launch_prefill_vs<D, 2>(qmap, kvmap, a, st);
-    return PA_ERR_UNSUPPORTED;
+    if constexpr (D == 64) {
+        return launch_prefill_stages<64, 3, 3>(qmap, kvmap, a, st);
+    } else {
+        if (prefill_smem<D, 3, 2>(a.B) <= kSmemLimit)
+            return launch_prefill_stages<D, 3, 2>(qmap, kvmap, a, st);
+        if (prefill_smem<D, 2, 2>(a.B) <= kSmemLimit)
+            return launch_prefill_stages<D, 2, 2>(qmap, kvmap, a, st);
+        return PA_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace
