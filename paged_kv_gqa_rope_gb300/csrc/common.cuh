@@ -90,6 +90,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Both phases: the two barriers are first tested together (a barrier's
+// state takes a round trip of about 150 cycles to read; two tests issued
+// back to back share it), and only one still incomplete is waited for.
+__device__ __forceinline__ bool mbar_wait2(uint64_t *b1, uint32_t p1, uint64_t *b2, uint32_t p2) {
+    uint32_t d1, d2;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q1, [%2], %3;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q2, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, q1;\n\t"
+        "selp.u32 %1, 1, 0, q2;\n\t}"
+        : "=r"(d1), "=r"(d2)
+        : "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+        : "memory");
+    if (d1 && d2) return true;
+    return (d1 || mbar_wait(b1, p1)) && (d2 || mbar_wait(b2, p2));
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {

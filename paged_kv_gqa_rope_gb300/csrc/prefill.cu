@@ -28,12 +28,16 @@
 // Pipeline.  Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, the score
 // tile of each query tile (128 keys) and its output accumulator.  Per key
 // tile the softmax of tile t reads S_t in two 64-column halves and writes
-// each half's P as fp16 over S_t's first columns, handing the first half to
-// the tensor core at once; O_t += P.V runs in the same two halves, and the
-// next key tile's S_t goes into the same TMEM after it.  Each query tile has
-// its own MMA thread, so one tile's softmax runs while the tensor core works
-// on the other's P.V and next scores, and neither tile's MMAs wait behind the
-// other's synchronisation.
+// each half's P as fp16 over the first 32 columns of the half, handing the
+// first half to the tensor core at once; O_t += P.V runs in the same two
+// halves, and each half of the next key tile's scores (N = 64) goes into
+// its half of S_t as soon as the P.V that reads that half's P is issued
+// (tcgen05.mma operations issued by one thread execute in issue order).
+// So the next tile's first-half scores are computed while the softmax works
+// on this tile's second half.  Each query tile has its own MMA thread, so
+// one tile's softmax runs while the tensor core works on the other's P.V
+// and scores, and neither tile's MMAs wait behind the other's
+// synchronisation.
 //
 // Roles (512 threads, 128 registers each):
 //   warps 0-3, 4-7   softmax of query tile 0 / 1 (thread i owns row i =
@@ -104,7 +108,7 @@ struct PrefillArgs {
 // Shared memory: a small area of barriers, the unit ring, row sums and the
 // sequence table at the start of the window (16-byte aligned), then, from
 // the next 1024-byte boundary (128-byte swizzle), the operand tiles.
-constexpr int kRingOff = 448;                    // barriers + TMEM slot before it
+constexpr int kRingOff = 464;                    // barriers + TMEM slot before it
 constexpr int kLsumOff = kRingOff + kRing * 32;  // float [2 tiles][128]: row sums
 constexpr int kTabOff = kLsumOff + 2 * 128 * 4;  // int4 [B + 1]: sequence table
 // int [B] after the table: sequence of each table row (ranked batches)
@@ -142,18 +146,19 @@ enum {
     B_VFULL = 10,   // up to 3 V stages
     B_VEMPTY = 13,  // up to 3
     B_VFIXED = 16,  // up to 3: a V tile whose tail rows were cleared
-    B_SFULL = 19,   // per query tile: scores written
-    B_PHALF = 21,   // per query tile: P of the first 64 keys written
-    B_PREADY = 23,  // per query tile: P of all 128 keys written
-    B_OHALF = 25,   // per query tile: the P.V of the first 64 keys done
-    B_OUNIT = 29,   // per query tile: the unit's last P.V done
-    B_OFREE = 31,   // per query tile: O_t read out
-    B_LREADY = 33,  // per query tile: row sums of a unit written
-    B_LFREE = 35,   // per query tile: row sums read
-    B_DRAIN = 37,   // per query tile
-    B_UFULL = 39,   // kRing: unit ring entry written
-    B_UEMPTY = 47,  // kRing: entry read by every consumer warp
-    B_COUNT = 55
+    B_SFULL = 19,   // [tile][half]: scores of the half written
+    B_PHALF = 23,   // per query tile: P of the first 64 keys written
+    B_PREADY = 25,  // per query tile: P of all 128 keys written
+    B_OHALF = 27,   // per query tile: the P.V of the first 64 keys done
+    B_ODONE = 29,   // per query tile: the P.V of the other 64 keys done
+    B_OUNIT = 31,   // per query tile: the unit's last P.V done
+    B_OFREE = 33,   // per query tile: O_t read out
+    B_LREADY = 35,  // per query tile: row sums of a unit written
+    B_LFREE = 37,   // per query tile: row sums read
+    B_DRAIN = 39,   // per query tile
+    B_UFULL = 41,   // kRing: unit ring entry written
+    B_UEMPTY = 49,  // kRing: entry read by every consumer warp
+    B_COUNT = 57
 };
 static_assert(B_COUNT * 8 + 4 <= kRingOff, "barrier area");
 
@@ -441,10 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar[B_QFULL + i], 1);
             mbar_init(&bar[B_QEMPTY + i], 1);
-            mbar_init(&bar[B_SFULL + i], 1);
+            mbar_init(&bar[B_SFULL + 2 * i], 1);
+            mbar_init(&bar[B_SFULL + 2 * i + 1], 1);
             mbar_init(&bar[B_PHALF + i], 128);
             mbar_init(&bar[B_PREADY + i], 128);
             mbar_init(&bar[B_OHALF + i], 1);
+            mbar_init(&bar[B_ODONE + i], 1);
             mbar_init(&bar[B_OUNIT + i], 1);
             mbar_init(&bar[B_OFREE + i], 128);
             mbar_init(&bar[B_LREADY + i], 128);
@@ -722,13 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 64 keys as soon as the softmax has written their P, then over the
         // other 64, then S_t(j + 1) = Q_t.K_(j+1)^T into the same TMEM (the
         // P.V was issued first by this thread: tcgen05.mma operations issued
-        // by one thread execute in issue order).  Each thread releases every
-        // K and V tile of the unit (a stage is refilled once both have), also
-        // those its tile does not need, after seeing it loaded: so neither
-        // thread can get a ring's depth ahead of the other.
+        // by one thread execute in issue order).
         const int t = warp == kMma1Warp ? 1 : 0;
         if (lane == 0) {
-            constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN, false, false);
+            constexpr uint32_t kIdescQK = tc::idesc_f16(kBM, kBN / 2, false, false);
             constexpr uint32_t kIdescPV = tc::idesc_f16(kBM, D, false, true);
             // Shared-memory descriptors of the operand buffers, built once; a
             // k-step only adds its byte offset / 16 to the start-address field.
@@ -740,80 +744,105 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0;    // score tiles of this query tile in earlier units
             int un = 0;   // earlier units with rows in this tile
             int fix0 = 0, fix1 = 0, fix2 = 0;  // cleared V tiles per V stage
-            // S_t = Q_t.K^T of K/V tile kvi (K stage kvi % KS).
-            auto issue_s = [&](int kvi) {
-                const uint64_t dk = dk0 + (uint64_t)(((kvi % KS) * L::kKVTile) >> 4);
+            // Scores of keys 64x .. 64x + 63 of K/V tile kvi (K stage kvi % KS)
+            // into columns 64x .. 64x + 63 of S_t.
+            auto issue_s = [&](int kvi, int x) {
+                const uint64_t dk =
+                    dk0 + (uint64_t)(((kvi % KS) * L::kKVTile + x * (kBN / 2) * 128) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc::mma_ss(tmem + s_col(t),
+                    tc::mma_ss(tmem + s_col(t) + x * (kBN / 2),
                                dq + (uint64_t)(((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4),
                                dk + (uint64_t)(((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4),
                                kIdescQK, kk > 0);
-                tc::commit(&bar[B_SFULL + t]);
+                tc::commit(&bar[B_SFULL + 2 * t + x]);
+            };
+            // Releases of K/V tile j of a unit: a tile used by both query
+            // tiles is released once by each thread, one used by this tile
+            // alone twice by this thread, so no thread waits for a tile it
+            // does not read.  (A thread releases a tile only after seeing it
+            // loaded, and the stage's next load needs both releases: neither
+            // thread can release a stage's next tile before the other has
+            // released the current one.)
+            auto release = [&](int full_bar, int j, int n, int n_o) {
+                if (j < n) tc::commit(&bar[full_bar]);
+                if (j < n && j >= n_o) tc::commit(&bar[full_bar]);
             };
             int ui = 0;  // ring entry
             for (UnitIter u = take0(0); u.valid(total_units) && ok; u = take0(++ui)) {
                 const int n = u.ps.tiles(t);
+                const int n_o = u.ps.tiles(1 - t);
                 const int nmax = u.nmax();
                 const bool fix_tail = u.fix_tail();
-                // ---- K tile 0: the tile's first scores
-                ok = mbar_wait(&bar[B_KFULL + kvc % KS], (kvc / KS) & 1);
-                if (ok && n > 0) ok = mbar_wait(&bar[B_QFULL + t], un & 1);
-                if (!ok) break;
-                tc::fence_after();
                 if (n > 0) {
-                    issue_s(kvc);
+                    // ---- K tile 0: the tile's first scores
+                    ok = mbar_wait(&bar[B_KFULL + kvc % KS], (kvc / KS) & 1) &&
+                         mbar_wait(&bar[B_QFULL + t], un & 1);
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_s(kvc, 0);
+                    issue_s(kvc, 1);
                     if (n == 1) tc::commit(&bar[B_QEMPTY + t]);  // Q_t done
+                    release(B_KEMPTY + kvc % KS, 0, n, n_o);
                 }
-                tc::commit(&bar[B_KEMPTY + kvc % KS]);
-                for (int j = 0; j < nmax && ok; ++j) {
+                for (int j = 0; j < n && ok; ++j) {
                     const int kvi = kvc + j;
                     const int vs = kvi % VS;
+                    const int G = g + j;  // this score tile
                     // V tile j (its tail rows cleared first when it holds the
                     // sequence's last block)
                     const bool fixed = fix_tail && j == nmax - 1;
-                    ok = fixed ? mbar_wait(&bar[B_VFIXED + vs],
-                                           (vs == 0 ? fix0 : vs == 1 ? fix1 : fix2) & 1)
-                               : mbar_wait(&bar[B_VFULL + vs], (kvi / VS) & 1);
-                    const bool next_k = j + 1 < nmax;
-                    if (ok && next_k)
+                    const bool next_s = j + 1 < n;
+                    ok = mbar_wait2(fixed ? &bar[B_VFIXED + vs] : &bar[B_VFULL + vs],
+                                    fixed ? (vs == 0 ? fix0 : vs == 1 ? fix1 : fix2) & 1
+                                          : (kvi / VS) & 1,
+                                    &bar[B_PHALF + t], G & 1);
+                    if (ok && next_s)
                         ok = mbar_wait(&bar[B_KFULL + (kvi + 1) % KS], ((kvi + 1) / KS) & 1);
+                    // The unit's first P.V overwrites O_t: the output warpgroup
+                    // must have read the previous unit's.
+                    if (ok && j == 0 && un > 0) ok = mbar_wait(&bar[B_OFREE + t], (un - 1) & 1);
                     if (!ok) break;
-                    if (j < n) {
-                        const int G = g + j;  // this score tile
-                        const uint64_t dv = dv0 + (uint64_t)((vs * L::kKVTile) >> 4);
-                        ok = mbar_wait(&bar[B_PHALF + t], G & 1);
-                        // The unit's first P.V overwrites O_t: the output
-                        // warpgroup must have read the previous unit's.
-                        if (ok && j == 0 && un > 0) ok = mbar_wait(&bar[B_OFREE + t], (un - 1) & 1);
-                        if (!ok) break;
-                        tc::fence_after();
+                    tc::fence_after();
+                    const uint64_t dv = dv0 + (uint64_t)((vs * L::kKVTile) >> 4);
+                    // P of the first 64 keys sits in columns 0 .. 31, of the
+                    // other 64 in columns 64 .. 95: each half of the next
+                    // scores can go in as soon as the P.V that reads the
+                    // half's P is issued
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 32; ++kk)
-                            tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kk * 8,
-                                       dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                        tc::commit(&bar[B_OHALF + t]);
-                        ok = mbar_wait(&bar[B_PREADY + t], G & 1);
-                        if (!ok) break;
-                        tc::fence_after();
+                    for (int kk = 0; kk < kBN / 32; ++kk)
+                        tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kk * 8,
+                                   dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::commit(&bar[B_OHALF + t]);
+                    if (next_s) issue_s(kvi + 1, 0);
+                    ok = mbar_wait(&bar[B_PREADY + t], G & 1);
+                    if (!ok) break;
+                    tc::fence_after();
 #pragma unroll
-                        for (int kk = kBN / 32; kk < kBN / 16; ++kk)
-                            tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kk * 8,
-                                       dv + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
-                        if (j == n - 1) tc::commit(&bar[B_OUNIT + t]);
-                        if (j + 1 < n) {  // the next scores, over P_t's TMEM
-                            issue_s(kvi + 1);
-                            if (j + 2 == n) tc::commit(&bar[B_QEMPTY + t]);  // Q_t done
-                        }
+                    for (int kk = 0; kk < kBN / 32; ++kk)
+                        tc::mma_ts(tmem + o_col(t, D), tmem + s_col(t) + kBN / 2 + kk * 8,
+                                   dv + (uint64_t)(((kBN / 2 + kk * 16) * 128) >> 4), kIdescPV, 1u);
+                    tc::commit(&bar[B_ODONE + t]);
+                    if (j == n - 1) tc::commit(&bar[B_OUNIT + t]);
+                    if (next_s) {
+                        issue_s(kvi + 1, 1);
+                        if (j + 2 == n) tc::commit(&bar[B_QEMPTY + t]);  // Q_t done
                     }
-                    tc::commit(&bar[B_VEMPTY + vs]);
-                    if (next_k) tc::commit(&bar[B_KEMPTY + (kvi + 1) % KS]);
+                    release(B_VEMPTY + vs, j, n, n_o);
+                    if (next_s) release(B_KEMPTY + (kvi + 1) % KS, j + 1, n, n_o);
                     if (fixed) {
                         fix0 += vs == 0;
                         fix1 += vs == 1;
                         fix2 += vs == 2;
                     }
+                }
+                // the unit's cleared V tile, when only the other tile reads it
+                if (ok && fix_tail && n < nmax) {
+                    const int vs = (kvc + nmax - 1) % VS;
+                    fix0 += vs == 0;
+                    fix1 += vs == 1;
+                    fix2 += vs == 2;
                 }
                 kvc += nmax;
                 if (n > 0) {
@@ -849,9 +878,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n && ok; ++j) {
                 const int G = g + j;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], G & 1));
-                if (!ok) break;
-                tc::fence_after();
                 const bool masked = j * kBN + kBN - 1 > first_row;
                 // Each 64-column half is read from TMEM once with its 32
                 // columns' maxima (tcgen05.ld.red; a masked half takes the
@@ -861,6 +887,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // while the second is computed).
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + 2 * t + hf], G & 1));
+                    if (!ok) break;
+                    tc::fence_after();
                     uint32_t sa[32], sb[32];
                     float ma, mb;
                     tc::ld32_max_issue(s_tmem + hf * 64, sa, ma);
@@ -883,15 +912,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O_t holds P.V made with the old maximum: it is scaled
                         // down to the new one by the whole warp (TMEM loads
                         // and stores are warp-wide; rows that keep their
-                        // maximum scale by 1).  For the first half that is the
-                        // earlier tiles' P.V, complete: this tile's scores were
-                        // issued after the last of them into the TMEM it read.
-                        // For the second half it also holds this tile's first
-                        // half P.V, waited for here.
-                        if (hf == 1) {
-                            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OHALF + t], G & 1));
-                            if (!ok) break;
-                        }
+                        // maximum scale by 1) once the P.V issued for the
+                        // half before this one is done: the previous tile's
+                        // second half for the first half, this tile's first
+                        // half for the second.  (The P.V before that one
+                        // completed before this half's scores, issued after it.)
+                        ok = __all_sync(0xffffffffu,
+                                        hf == 0 ? mbar_wait(&bar[B_ODONE + t], (G - 1) & 1)
+                                                : mbar_wait(&bar[B_OHALF + t], G & 1));
+                        if (!ok) break;
                         tc::fence_after();
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
@@ -906,8 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t la = 0, lb = 0;  // packed partial row sums (+0.0f pairs)
                         uint32_t pa[16], pb[16];
                         exp_half(sa, sb, sl2x2, m_used, pa, pb, la, lb);
-                        tc::st16(s_tmem + hf * 32, pa);
-                        tc::st16(s_tmem + hf * 32 + 16, pb);
+                        // P of this half over the first 32 of its 64 columns
+                        tc::st16(s_tmem + hf * 64, pa);
+                        tc::st16(s_tmem + hf * 64 + 16, pb);
                         float x0, x1, y0, y1;
                         f2_unpack(la, x0, x1);
                         f2_unpack(lb, y0, y1);
