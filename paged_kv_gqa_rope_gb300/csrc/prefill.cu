@@ -232,7 +232,11 @@ __device__ __forceinline__ void exp_half(const uint32_t (&sa)[32], const uint32_
 }
 
 // Shape of row pair k of a sequence with L_q query rows and a prefix of p.
+// When L_q is not a multiple of 256 the odd rows form the first pair (rows
+// 0 .. L_q mod 256 - 1): a pair with an empty or short second tile then
+// sees the fewest keys, instead of the most as the sequence's last rows.
 struct PairShape {
+    int q0;     // first row of the pair
     int rv[2];  // valid rows of query tile 0 / 1
     int n[2];   // key tiles of query tile 0 / 1 (0 for an empty tile)
     // Selects instead of a run-time index keep the shape in registers.
@@ -242,11 +246,14 @@ struct PairShape {
 
 __device__ __forceinline__ PairShape pair_shape(int p, int L_q, int k) {
     PairShape ps;
-    const int q0 = k * kUnitRows;
-    ps.rv[0] = min(kBM, L_q - q0);
-    ps.rv[1] = max(0, min(kBM, L_q - q0 - kBM));
-    ps.n[0] = (p + q0 + ps.rv[0] + kBN - 1) / kBN;
-    ps.n[1] = ps.rv[1] > 0 ? (p + q0 + kBM + ps.rv[1] + kBN - 1) / kBN : 0;
+    const int rem = L_q % kUnitRows;
+    const int off = rem == 0 ? 0 : rem - kUnitRows;  // where pair 0 would start
+    ps.q0 = max(0, off + k * kUnitRows);
+    const int rows = off + (k + 1) * kUnitRows - ps.q0;
+    ps.rv[0] = min(kBM, rows);
+    ps.rv[1] = max(0, rows - kBM);
+    ps.n[0] = (p + ps.q0 + ps.rv[0] + kBN - 1) / kBN;
+    ps.n[1] = ps.rv[1] > 0 ? (p + ps.q0 + kBM + ps.rv[1] + kBN - 1) / kBN : 0;
     return ps;
 }
 
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const bool row_valid = r < u.ps.rows(t);
                 uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.out + ((int64_t)(u.si.q_begin + u.k * kUnitRows + t * kBM + r) * a.H + u.h) * D);
+                    a.out + ((int64_t)(u.si.q_begin + u.ps.q0 + t * kBM + r) * a.H + u.h) * D);
                 // 32 columns at a time; O_t is released once its last columns
                 // are read.
 #pragma unroll
@@ -610,11 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (v.u >= total_units) {
                     sched_finish(a.sched);
                 } else {
-                    const int rows = min(kUnitRows, v.si.L_q - v.k * kUnitRows);
-                    for (int t = 0; t < 2 && t * kBM < rows; ++t)
+                    const PairShape ps = pair_shape(v.si.k_len - v.si.L_q, v.si.L_q, v.k);
+                    for (int t = 0; t < 2 && ps.rows(t) > 0; ++t)
                         for (int hf = 0; hf < D / 64; ++hf)
-                            tma_prefetch_4d(&qmap, 0, hf, v.h,
-                                            v.si.q_begin + v.k * kUnitRows + t * kBM);
+                            tma_prefetch_4d(&qmap, 0, hf, v.h, v.si.q_begin + ps.q0 + t * kBM);
                 }
             }
             ok = __shfl_sync(0xffffffffu, okw, 0) && ok;
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!is_v) un = schedule(ui + 1);
             const int nmax = u.nmax();
             const int kvh = u.h / a.g;
-            const int q0 = u.k * kUnitRows;
+            const int q0 = u.ps.q0;
             const bool fix_tail = is_v && u.fix_tail();
             for (int j = 0; j < nmax && ok; ++j) {
                 int rows_next;
@@ -873,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (UnitIter u = take(0); u.valid(total_units) && ok; u = take(++ui)) {
             const int n = u.ps.tiles(t);
             if (n == 0) continue;
-            const int first_row = u.p + u.k * kUnitRows + t * kBM;  // position of row 0
+            const int first_row = u.p + u.ps.q0 + t * kBM;  // position of row 0
             const int key_lim = min(first_row + r, u.si.k_len - 1);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n && ok; ++j) {
