@@ -84,7 +84,7 @@ constexpr int kThreads = 16 * 32;  // 128 registers per thread
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxSeqs = 2048;
-constexpr int kRing = 8;             // scheduled units buffered per CTA
+constexpr int kRing = 6;             // scheduled units buffered per CTA
 constexpr int kRingConsumers = 15;   // warps that read every ring entry
 constexpr int kSchedSlots = 64;      // launches that may run at the same time
 
@@ -108,8 +108,9 @@ struct PrefillArgs {
 // Shared memory: a small area of barriers, the unit ring, row sums and the
 // sequence table at the start of the window (16-byte aligned), then, from
 // the next 1024-byte boundary (128-byte swizzle), the operand tiles.
-constexpr int kRingOff = 464;                    // barriers + TMEM slot before it
-constexpr int kLsumOff = kRingOff + kRing * 32;  // float [2 tiles][128]: row sums
+constexpr int kRingOff = 432;                    // barriers + TMEM slot before it
+constexpr int kSeenOff = kRingOff + kRing * 32;  // int [8]: K / V tiles seen per stage
+constexpr int kLsumOff = kSeenOff + 32;          // float [2 tiles][128]: row sums
 constexpr int kTabOff = kLsumOff + 2 * 128 * 4;  // int4 [B + 1]: sequence table
 // int [B] after the table: sequence of each table row (ranked batches)
 __host__ __device__ __forceinline__ int misc_bytes(int B, bool ranked) {
@@ -157,10 +158,36 @@ enum {
     B_LFREE = 37,   // per query tile: row sums read
     B_DRAIN = 39,   // per query tile
     B_UFULL = 41,   // kRing: unit ring entry written
-    B_UEMPTY = 49,  // kRing: entry read by every consumer warp
-    B_COUNT = 57
+    B_UEMPTY = 47,  // kRing: entry read by every consumer warp
+    B_COUNT = 53
 };
+static_assert(B_UEMPTY == B_UFULL + kRing && B_COUNT == B_UEMPTY + kRing, "ring barriers");
 static_assert(B_COUNT * 8 + 4 <= kRingOff, "barrier area");
+
+// Highest K or V tile of a stage that an MMA thread has seen land: written
+// with release order after the thread's wait on the tile's barrier, read
+// with acquire order, and only ever raised, so (unlike a barrier's phase
+// parity) a value cannot be mistaken for an older one.
+__device__ __forceinline__ void seen_raise(int *p, int tile) {
+    asm volatile("red.release.cta.shared::cta.max.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(tile)
+                 : "memory");
+}
+__device__ __forceinline__ int seen_read(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+// Until tile `tile` of the stage has been seen to land (false after
+// kWaitLimitNs).
+__device__ __forceinline__ bool seen_wait(const int *p, int tile) {
+    if (seen_read(p) >= tile) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (seen_read(p) < tile) {
+        __nanosleep(64);
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2, int c3) {
@@ -466,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar[B_DRAIN], 1);
         mbar_init(&bar[B_DRAIN + 1], 1);
+        for (int i = 0; i < 8; ++i) reinterpret_cast<int *>(smem_raw + kSeenOff)[i] = -1;
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&bar[B_UFULL + i], 1);
             mbar_init(&bar[B_UEMPTY + i], kRingConsumers);
@@ -774,6 +802,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j < n) tc::commit(&bar[full_bar]);
                 if (j < n && j >= n_o) tc::commit(&bar[full_bar]);
             };
+            // A wait on a stage barrier by phase parity is exact only while
+            // the barrier's previous phase is complete (the next cannot
+            // complete before this thread releases the tile).  A thread that
+            // skipped the stage's previous tile (the other query tile's last
+            // key tile, or a unit with no rows of this tile) has not seen it
+            // land: it would pass at once while that load is still in flight.
+            // So before such a wait it checks the stage's seen counter, which
+            // both threads raise after each wait.  The previous tile of a
+            // stage lies in an earlier unit only for the first KS (or VS)
+            // tiles of a unit; for K tile 0 the Q wait below gives the same.
+            int *const kseen = reinterpret_cast<int *>(smem_raw + kSeenOff);
+            int *const vseen = kseen + 4;
             int ui = 0;  // ring entry
             for (UnitIter u = take0(0); u.valid(total_units) && ok; u = take0(++ui)) {
                 const int n = u.ps.tiles(t);
@@ -782,9 +822,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool fix_tail = u.fix_tail();
                 if (n > 0) {
                     // ---- K tile 0: the tile's first scores
-                    ok = mbar_wait(&bar[B_KFULL + kvc % KS], (kvc / KS) & 1) &&
-                         mbar_wait(&bar[B_QFULL + t], un & 1);
+                    // (Q_t first: the producer loads a unit's Q tiles only
+                    // after its K tile 0, whose stage it takes only once the
+                    // stage's previous tile has landed and been released, so
+                    // the parity wait on K tile 0 that follows is exact)
+                    ok = mbar_wait(&bar[B_QFULL + t], un & 1) &&
+                         mbar_wait(&bar[B_KFULL + kvc % KS], (kvc / KS) & 1);
                     if (!ok) break;
+                    seen_raise(kseen + kvc % KS, kvc);
                     tc::fence_after();
                     issue_s(kvc, 0);
                     issue_s(kvc, 1);
@@ -799,12 +844,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // sequence's last block)
                     const bool fixed = fix_tail && j == nmax - 1;
                     const bool next_s = j + 1 < n;
-                    ok = mbar_wait2(fixed ? &bar[B_VFIXED + vs] : &bar[B_VFULL + vs],
-                                    fixed ? (vs == 0 ? fix0 : vs == 1 ? fix1 : fix2) & 1
-                                          : (kvi / VS) & 1,
-                                    &bar[B_PHALF + t], G & 1);
-                    if (ok && next_s)
-                        ok = mbar_wait(&bar[B_KFULL + (kvi + 1) % KS], ((kvi + 1) / KS) & 1);
+                    if (j < VS && kvi >= VS) ok = seen_wait(vseen + vs, kvi - VS);
+                    ok = ok && mbar_wait2(fixed ? &bar[B_VFIXED + vs] : &bar[B_VFULL + vs],
+                                          fixed ? (vs == 0 ? fix0 : vs == 1 ? fix1 : fix2) & 1
+                                                : (kvi / VS) & 1,
+                                          &bar[B_PHALF + t], G & 1);
+                    if (ok) seen_raise(vseen + vs, kvi);
+                    if (ok && next_s) {
+                        const int kn = kvi + 1;
+                        if (j + 1 < KS && kn >= KS) ok = seen_wait(kseen + kn % KS, kn - KS);
+                        ok = ok && mbar_wait(&bar[B_KFULL + kn % KS], (kn / KS) & 1);
+                        if (ok) seen_raise(kseen + kn % KS, kn);
+                    }
                     // The unit's first P.V overwrites O_t: the output warpgroup
                     // must have read the previous unit's.
                     if (ok && j == 0 && un > 0) ok = mbar_wait(&bar[B_OFREE + t], (un - 1) & 1);
@@ -1026,17 +1077,15 @@ int launch_prefill_stages(const CUtensorMap &qmap, const CUtensorMap &kvmap,
     return launch_status();
 }
 
-// Ring depths at head_dim 128: three K stages and two V stages when the
-// batch's sequence table leaves room for them, two and two otherwise; at
-// head_dim 64 the tiles are half the size and both rings get three.
+// Ring depths: two K and two V stages at head_dim 128 (a third stage of
+// either fits only for small batches and measured slower on the 16-sequence
+// prefill), three of each at head_dim 64, where the tiles are half the size.
 template <int D>
 int launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kvmap, const PrefillArgs &a,
                    cudaStream_t st) {
     if constexpr (D == 64) {
         return launch_prefill_stages<64, 3, 3>(qmap, kvmap, a, st);
     } else {
-        if (prefill_smem<D, 3, 2>(a.B) <= kSmemLimit)
-            return launch_prefill_stages<D, 3, 2>(qmap, kvmap, a, st);
         if (prefill_smem<D, 2, 2>(a.B) <= kSmemLimit)
             return launch_prefill_stages<D, 2, 2>(qmap, kvmap, a, st);
         return PA_ERR_UNSUPPORTED;

@@ -176,8 +176,8 @@ def test_prefill_bad_lengths_are_reported():
 
 
 def test_prefill_many_sequences():
-    """A batch large enough that the kernel keeps two V stages (its
-    per-sequence table takes the third stage's shared memory)."""
+    """300 sequences: a 300-row sequence table in shared memory and many
+    short units handed out by the work counter."""
     rng = np.random.default_rng(41)
     B = 300
     cached = rng.integers(0, 60, size=B).tolist()
@@ -216,3 +216,36 @@ def test_prefill_rising_maximum_rescales():
             blk, row = case.block_tables[s][p // 16], p % 16
             init[0, 0, blk, row] = (init[0, 0, blk, row].astype(np.float32) * grow(p)).astype(np.float16)
     check(case, init)
+
+
+@pytest.mark.parametrize("shape", ["prefill_13b", "skips"])
+def test_prefill_repeats_bit_for_bit(shape):
+    """The same launch thirty times gives the same bits.  The two query
+    tiles of a unit share K/V stages; a tile skips the key tiles only the
+    other one reads (the last key tile of a pair, every key tile of a first
+    pair whose second tile is empty), and a stage it skipped must have been
+    seen to land before it waits for the stage's next load.  "skips" makes
+    such pairs common: query lengths that leave L_q mod 256 in 1..128, with
+    prefixes of one to three key tiles."""
+    if shape == "prefill_13b":
+        case = W.make_case("prefill_13b")
+        init = W.initial_cache(case)
+    else:
+        rng = np.random.default_rng(61)
+        B = 24
+        new = (256 * rng.integers(0, 4, size=B) + rng.integers(1, 129, size=B)).tolist()
+        cached = (16 * rng.integers(8, 24, size=B)).tolist()
+        case, init = custom_prefill_case(16, 4, 128, cached, new, seed=62)
+    run = PrefillRun(case, init)
+    first = run.run().clone()
+    assert int(run.status.item()) == 0
+    wl = case.wl
+    for i in range(30):
+        out = pa.prefill_varlen(run.q, run.cache, run.cuq, run.cuk, run.bt,
+                                run.md["max_seqlen_q"], wl.n_kv_heads, status=run.status)
+        torch.cuda.synchronize()
+        assert torch.equal(out, first), f"launch {i + 1} differs from the first"
+    assert int(run.status.item()) == 0
+    if shape == "skips":
+        _, _, want, _ = oracle_prefill(case, init)
+        assert_attention_close(first, want)
