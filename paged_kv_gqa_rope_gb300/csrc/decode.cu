@@ -5,16 +5,22 @@
 // "Meta Llama source deep-dive", 3.4 repeat_kv: Q head h reads KV head h/g).
 //
 // Work decomposition.  Every (sequence s, KV head h) pair owns
-// ceil(context_lens[s] / 16) KV blocks; laid end to end, pair after pair,
-// they form one line of W blocks.  The persistent grid of G CTAs cuts that
-// line into G equal ranges, so every CTA streams the same number of bytes
-// whatever the mix of context lengths.  A CTA walks its range as segments
-// (the part of one pair that falls in it).  A pair that lies inside one
-// range is finished there; a pair cut by range ends is finished by the CTA
-// that completes its last piece: each piece leaves (max, sum, unnormalised
-// O) in the workspace (record slot 0 if it is the CTA's first segment, 1 if
-// its last), and the last to arrive merges the 2-3 pieces by an online
-// softmax and resets the pair's arrival counter to zero.
+// ceil(context_lens[s] / 16) KV blocks followed by kPairCost units that
+// stand for the pair's fixed cost (its merge and output, about the time of
+// four blocks' streaming); laid end to end, pair after pair, they form one
+// line of W units.  The persistent grid of G CTAs cuts that line into G equal
+// ranges, so every CTA has about the same work whatever the mix of context
+// lengths (a CTA with many short pairs streams fewer blocks).  A CTA walks
+// its range as segments (the part of one pair that falls in it; a segment
+// of a pair's cost units alone has no block and is skipped).  A pair whose
+// blocks lie inside one range is finished there; a pair whose blocks are cut
+// by range ends is finished by the CTA that completes its last piece: each
+// piece leaves (max, sum, unnormalised O) in the workspace (record slot 0 if
+// it is the CTA's first segment, 1 if its last), and the last to arrive
+// merges the 2-3 pieces by an online softmax and resets the pair's arrival
+// counter to zero; if the pieces of the others have all arrived when a CTA
+// reaches the end of its last segment, that CTA closes the pair from its own
+// partial results without leaving a record.
 //
 // Inside a CTA one producer warp streams the K and V block tiles (16 tokens x
 // head_dim fp16 of one KV head; one TMA copy brings both) into a ring of
@@ -94,9 +100,15 @@ __device__ __forceinline__ int cta_of(int64_t idx, int64_t W, int G) {
     return (int)(((idx + 1) * G + W - 1) / W) - 1;
 }
 
-// Segment of the block line starting at `pos` (< end): its pair and blocks.
+// Units of the line that stand for one pair's fixed cost.
+constexpr int kPairCost = 4;
+
+// Segment of the line starting at `pos` (< end): its pair, its nu units and
+// the nb blocks among them (blocks b0 .. b0 + nb - 1 of the pair, nb = 0 for
+// a segment of cost units alone); the pair's blocks are the units
+// [pair_start, pair_end).
 struct Segment {
-    int s, kvh, b0, nb, ctx;
+    int s, kvh, b0, nb, nu, ctx;
     int64_t pair_start, pair_end;
 };
 
@@ -114,12 +126,15 @@ __device__ __forceinline__ Segment segment_at(int64_t pos, int64_t end, const in
     g.s = lo;
     g.ctx = __ldg(context_lens + lo);
     const int nblk = (g.ctx + kBlockSize - 1) / kBlockSize;
+    const int span = nblk + kPairCost;
     const int64_t rem = pos - prefix[lo];
-    g.kvh = (int)(rem / nblk);
-    g.b0 = (int)(rem - (int64_t)g.kvh * nblk);
-    g.pair_start = prefix[lo] + (int64_t)g.kvh * nblk;
+    g.kvh = (int)(rem / span);
+    const int u0 = (int)(rem - (int64_t)g.kvh * span);  // unit of the pair
+    g.pair_start = prefix[lo] + (int64_t)g.kvh * span;
     g.pair_end = g.pair_start + nblk;
-    g.nb = (int)(min(end, g.pair_end) - pos);
+    g.nu = (int)(min(end, g.pair_start + span) - pos);
+    g.b0 = min(u0, nblk);
+    g.nb = max(0, min(u0 + g.nu, nblk) - u0);
     return g;
 }
 
@@ -173,21 +188,100 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 // M = max_i m_i; f_i = 2^(m_i - M) replaces m_i (all zero when every m_i is
 // -inf, an empty part); L = sum_i f_i l_i goes to l[h] and M to
 // l[kGroupPad + h].  O = sum_i f_i O_i is then the merged numerator.
+// Every merge of partial results (warps, pieces) sums in index order with
+// explicit fused multiply-adds, so a pair's output has the same bits
+// whichever CTA, and which of the merge paths, combines its pieces.
+__device__ __forceinline__ float piece_factor(float m, float M) {
+    return M == -INFINITY ? 0.f : ex2(m - M);
+}
 __device__ __forceinline__ void merge_factors(float *m, float *l, int h, int n) {
     float M = -INFINITY;
     for (int i = 0; i < n; ++i) M = fmaxf(M, m[i * kGroupPad + h]);
     float Lsum = 0.f;
     for (int i = 0; i < n; ++i) {
-        const float f = M == -INFINITY ? 0.f : ex2(m[i * kGroupPad + h] - M);
+        const float f = piece_factor(m[i * kGroupPad + h], M);
         m[i * kGroupPad + h] = f;
-        Lsum += f * l[i * kGroupPad + h];
+        Lsum = __fmaf_rn(f, l[i * kGroupPad + h], Lsum);
     }
     l[h] = Lsum;
     l[kGroupPad + h] = M;
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The pair's output rows from its pieces' records, by one warp (the warp of
+// the last piece to arrive, while the rest of its CTA goes on).  Per head:
+// the pieces' maximum M (lanes load the pieces' maxima together), then, for
+// pieces in groups of 32 (lane j holding piece i0 + j's factor 2^(m - M) and
+// sum), the row sum and the O of the head's D columns (lane = column within
+// each run of 32) accumulated in piece order, the O values of four pieces
+// loaded at a time (two for the int8 kernel, whose registers are capped).
+template <int D, bool I8>
+__device__ void warp_merge_records(const DecodeArgs &a, const Segment &sg, int64_t W, int G,
+                                   int lane) {
+    constexpr int kRec = D + 4;
+    constexpr int kRuns = D / 32;
+    constexpr int kBatch = I8 ? 2 : 4;
+    const int c_first = cta_of(sg.pair_start, W, G), c_last = cta_of(sg.pair_end - 1, W, G);
+    const int nrec = c_last - c_first + 1;
+    auto rec_of = [&](int i, int h) -> const float * {
+        const int c = c_first + i;
+        const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+        return a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * kRec;
+    };
+    for (int h = 0; h < a.g; ++h) {
+        float M = -INFINITY;
+        for (int i0 = 0; i0 < nrec; i0 += 32)
+            if (i0 + lane < nrec) M = fmaxf(M, __ldcg(rec_of(i0 + lane, h) + D));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float Lsum = 0.f;
+        float O[kRuns];
+#pragma unroll
+        for (int r = 0; r < kRuns; ++r) O[r] = 0.f;
+        for (int i0 = 0; i0 < nrec; i0 += 32) {
+            const int n = min(32, nrec - i0);
+            float fi = 0.f, li = 0.f;
+            if (lane < n) {
+                const float *r = rec_of(i0 + lane, h);
+                fi = piece_factor(__ldcg(r + D), M);
+                li = __ldcg(r + D + 1);
+            }
+            for (int j0 = 0; j0 < n; j0 += kBatch) {
+                float x[kBatch][kRuns];
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj) {
+                    const float *r = rec_of(i0 + min(j0 + jj, n - 1), h);
+#pragma unroll
+                    for (int rr = 0; rr < kRuns; ++rr)
+                        x[jj][rr] = j0 + jj < n ? __ldcg(r + rr * 32 + lane) : 0.f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj) {
+                    const float f = __shfl_sync(0xffffffffu, fi, (j0 + jj) & 31);
+                    const float l = __shfl_sync(0xffffffffu, li, (j0 + jj) & 31);
+                    if (j0 + jj < n) {
+                        Lsum = __fmaf_rn(f, l, Lsum);
+#pragma unroll
+                        for (int rr = 0; rr < kRuns; ++rr) O[rr] = __fmaf_rn(f, x[jj][rr], O[rr]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < kRuns; ++rr)
+            a.out[((int64_t)sg.s * a.H + sg.kvh * a.g + h) * D + rr * 32 + lane] =
+                __float2half_rn(Lsum > 0.f ? O[rr] / Lsum : 0.f);
+    }
+}
+
 template <int D, int NSTAGE, bool I8>
-__global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
+__global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap kvmap,
                   const __grid_constant__ CUtensorMap smap, const DecodeArgs a) {
     // Consumer warp w takes blocks w, w+4, ... of a segment, and segments end
@@ -210,7 +304,9 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
     float *sm_o = reinterpret_cast<float *>(stage_bad + NSTAGE);  // [4][8][D]
     float *sm_m = sm_o + kConsumerWarps * kGroupPad * D;           // [4][8]
     float *sm_l = sm_m + kConsumerWarps * kGroupPad;               // [4][8]
-    int *sm_flag = reinterpret_cast<int *>(sm_l + kConsumerWarps * kGroupPad);  // [4]
+    float *sm_pm = sm_l + kConsumerWarps * kGroupPad;              // [4][8] pieces' (max,
+    float *sm_pl = sm_pm + kConsumerWarps * kGroupPad;             // [4][8]  sum) per head
+    int *sm_flag = reinterpret_cast<int *>(sm_pl + kConsumerWarps * kGroupPad);  // [4]
     int64_t *prefix = reinterpret_cast<int64_t *>(sm_flag + 4);    // [B + 1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -222,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
         const int ctx = __ldg(a.context_lens + s);
         int64_t n = 0;
         if (ctx >= 1 && ctx <= a.maxb * kBlockSize)
-            n = (int64_t)((ctx + kBlockSize - 1) / kBlockSize) * a.Hk;
+            n = (int64_t)((ctx + kBlockSize - 1) / kBlockSize + kPairCost) * a.Hk;
         else if (cta == 0)
             report(a.status, PA_DEV_BAD_LENGTH);
         prefix[s + 1] = n;
@@ -318,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
                     ++gblk;
                 }
             }
-            pos += sg.nb;
+            pos += sg.nu;
         }
         // Leave no copy in flight: wait (bounded) for the last stages issued.
         if (lane == 0) {
@@ -337,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
     for (int64_t pos = start; pos < end;) {
         const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
         const int s = sg.s, kvh = sg.kvh, b0 = sg.b0, nb = sg.nb, ctx = sg.ctx;
+        if (nb == 0) {  // cost units alone
+            pos += sg.nu;
+            continue;
+        }
 
         // Q^T fragments (B operand).  fp16 cache: Q[head][16kk + 2*quad + {0,1}]
         // and + 8.  int8 cache: the k order of the K fragments built from the
@@ -626,125 +726,189 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
                 ow[D + d + 8] = o[mt][3];
             }
         }
+        const bool whole = pos == sg.pair_start && pos + nb == sg.pair_end;
+        // A cut pair: its pieces are those of CTAs c_first .. c_last.  On the
+        // CTA's last segment, if every other piece has already arrived on the
+        // pair's counter, this piece is the last, and the pair is merged from
+        // this CTA's partial results and the other pieces' records, with no
+        // record, fence or arrival of its own.  (The counter is read here; its
+        // value is needed after the barrier.)
+        int c_first = 0, c_last = 0, nrec = 1, arrived = -1;
+        bool may_close = false;
+        if (!whole) {
+            c_first = cta_of(sg.pair_start, W, G);
+            c_last = cta_of(sg.pair_end - 1, W, G);
+            nrec = c_last - c_first + 1;
+            may_close = pos + sg.nu == end && nrec <= kConsumerWarps;
+            if (may_close && tid == 0) arrived = ld_acquire_gpu(a.counters + s * a.Hk + kvh);
+        }
         named_barrier_sync(1, kCons);
         abort = sm_flag[1] != 0;
         if (tid < a.g) merge_factors(sm_m, sm_l, tid, kConsumerWarps);
+        if (tid == 0) sm_flag[2] = may_close && arrived == nrec - 1;
         named_barrier_sync(1, kCons);
+        const bool close = sm_flag[2] != 0;
+        const bool last_seg = pos + sg.nu == end;
 
-        const bool whole = pos == sg.pair_start && pos + nb == sg.pair_end;
-        const int slot = pos == start ? 0 : 1;
-        float *myrec = a.rec + ((int64_t)(cta * 2 + slot) * kGroupPad) * L::kRec;
-        for (int idx = tid; idx < a.g * D; idx += kCons) {
-            const int h = idx / D, d = idx - (idx / D) * D;
-            float O = 0.f;
+        if (whole) {
+            for (int idx = tid; idx < a.g * D; idx += kCons) {
+                const int h = idx / D, d = idx - (idx / D) * D;
+                float O = 0.f;
 #pragma unroll
-            for (int wv = 0; wv < kConsumerWarps; ++wv)
-                O += sm_m[wv * kGroupPad + h] * sm_o[(wv * kGroupPad + h) * D + d];
-            const float Lsum = sm_l[h];
-            if (whole) {
+                for (int wv = 0; wv < kConsumerWarps; ++wv)
+                    O = __fmaf_rn(sm_m[wv * kGroupPad + h], sm_o[(wv * kGroupPad + h) * D + d], O);
+                const float Lsum = sm_l[h];
                 a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
                     __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
-            } else {
-                float *r = myrec + h * L::kRec;
-                r[d] = O;
-                if (d == 0) {
-                    r[D] = sm_l[kGroupPad + h];
-                    r[D + 1] = Lsum;
-                }
             }
-        }
-        if (!whole) {
-            __threadfence();
-            named_barrier_sync(1, kCons);
-            const int c_first = cta_of(sg.pair_start, W, G);
-            const int c_last = cta_of(sg.pair_end - 1, W, G);
-            if (tid == 0) {
-                const int prev = atomicAdd(a.counters + s * a.Hk + kvh, 1);
-                sm_flag[0] = (prev == c_last - c_first);
-            }
-            named_barrier_sync(1, kCons);
-            const int nrec = c_last - c_first + 1;  // pieces of the pair
-            if (sm_flag[0] && nrec <= kConsumerWarps) {
-                // Merge of up to 4 pieces.  Each thread loads the O values of
-                // its (head, column) elements of every piece together, beside
-                // the pieces' (max, sum) per head, so the merge costs one or
-                // two L2 round trips; the factors per (piece, head) are
-                // computed once, in shared memory (the [4][8] areas are free).
-                __threadfence();
-                const float *pb[kConsumerWarps];
+            named_barrier_sync(1, kCons);  // the smem merge area is free again
+        } else {
+            // A piece of a cut pair.  Unless it closes the pair, it leaves the
+            // CTA's record of it (slot 0 for the CTA's first segment, 1 for its
+            // last) and arrives on the pair's counter after a release fence
+            // (one thread, after the barrier that follows every thread's
+            // record stores); the piece that arrives last merges the pair.
+            bool merge = close;
+            if (!close) {
+                const int slot = pos == start ? 0 : 1;
+                float *myrec = a.rec + ((int64_t)(cta * 2 + slot) * kGroupPad) * L::kRec;
+                for (int idx = tid; idx < a.g * D; idx += kCons) {
+                    const int h = idx / D, d = idx - (idx / D) * D;
+                    float O = 0.f;
 #pragma unroll
-                for (int i = 0; i < kConsumerWarps; ++i) {
-                    const int c = c_first + (i < nrec ? i : 0);
-                    const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                    pb[i] = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
+                    for (int wv = 0; wv < kConsumerWarps; ++wv)
+                        O = __fmaf_rn(sm_m[wv * kGroupPad + h], sm_o[(wv * kGroupPad + h) * D + d],
+                                      O);
+                    float *r = myrec + h * L::kRec;
+                    r[d] = O;
+                    if (d == 0) {
+                        r[D] = sm_l[kGroupPad + h];
+                        r[D + 1] = sm_l[h];
+                    }
                 }
-                // Elements tid + k * kCons; the int8 kernel (register count
-                // capped for four CTAs per SM) loads them all in one pass, the
-                // fp16 one in passes of four (two CTAs per SM need <= 168
-                // registers a thread).
+                named_barrier_sync(1, kCons);
+                if (!last_seg) {
+                    // Mid-range: warp 0 alone arrives (and, in the rare case
+                    // that this piece is the last, merges the pair from the
+                    // records) while the other warps go on with the next
+                    // segment.
+                    if (warp == 0) {
+                        int last = 0;
+                        if (lane == 0) {
+                            fence_acq_rel_gpu();
+                            const int prev = atomicAdd(a.counters + s * a.Hk + kvh, 1);
+                            last = prev == nrec - 1;
+                            if (last) fence_acq_rel_gpu();
+                        }
+                        if (__shfl_sync(0xffffffffu, last, 0)) {
+                            warp_merge_records<D, I8>(a, sg, W, G, lane);
+                            if (lane == 0) a.counters[s * a.Hk + kvh] = 0;
+                        }
+                    }
+                } else {
+                    // The CTA's last segment: every warp waits for the arrival.
+                    if (tid == 0) {
+                        fence_acq_rel_gpu();
+                        const int prev = atomicAdd(a.counters + s * a.Hk + kvh, 1);
+                        const int last = prev == nrec - 1;
+                        if (last) fence_acq_rel_gpu();
+                        sm_flag[0] = last;
+                    }
+                    named_barrier_sync(1, kCons);
+                    merge = sm_flag[0] != 0;
+                }
+            }
+            if (merge && nrec <= kConsumerWarps) {
+                // Pieces i = 0 .. nrec-1 of the pair (CTA c_first + i), from
+                // their records, except this CTA's own when it closes the pair:
+                // (max, sum) per head from the merge factors above, O from the
+                // four warps' partial O.  Each thread loads the records' O
+                // values of its elements first, then their (max, sum), so the
+                // loads overlap.
+                const int own = close ? cta - c_first : -1;
+                // Elements tid + k * kCons, in one pass (fp16) or passes of
+                // two (int8, whose registers are capped for four CTAs per SM).
                 constexpr int kEl = kGroupPad * D / kCons;
-                constexpr int kPass = I8 || kEl < 4 ? kEl : 4;
-                if (tid < nrec * a.g) {
-                    const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
-                    const float *r = pb[i] + h * L::kRec;
-                    sm_m[i * kGroupPad + h] = __ldcg(r + D);
-                    sm_l[i * kGroupPad + h] = __ldcg(r + D + 1);
-                }
+                constexpr int kPass = I8 && kEl > 2 ? 2 : kEl;
 #pragma unroll 1
                 for (int k0 = 0; k0 < kEl; k0 += kPass) {
                     float x[kConsumerWarps][kPass];
 #pragma unroll
                     for (int i = 0; i < kConsumerWarps; ++i) {
+                        const int c = c_first + i;
+                        const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                        const float *pb = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
 #pragma unroll
                         for (int k = 0; k < kPass; ++k) {
                             const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
-                            x[i][k] = i < nrec && idx < a.g * D
-                                          ? __ldcg(pb[i] + h * L::kRec + d)
+                            x[i][k] = i < nrec && i != own && idx < a.g * D
+                                          ? __ldcg(pb + h * L::kRec + d)
                                           : 0.f;
                         }
                     }
                     if (k0 == 0) {
+                        if (tid < nrec * a.g) {
+                            const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
+                            float pm, pl;
+                            if (i == own) {
+                                pm = sm_l[kGroupPad + h];
+                                pl = sm_l[h];
+                            } else {
+                                const int c = c_first + i;
+                                const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                                const float *r =
+                                    a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                                pm = __ldcg(r + D);
+                                pl = __ldcg(r + D + 1);
+                            }
+                            sm_pm[i * kGroupPad + h] = pm;
+                            sm_pl[i * kGroupPad + h] = pl;
+                        }
                         named_barrier_sync(1, kCons);
-                        if (tid < a.g) merge_factors(sm_m, sm_l, tid, nrec);
+                        if (tid < a.g) merge_factors(sm_pm, sm_pl, tid, nrec);
                         named_barrier_sync(1, kCons);
                     }
 #pragma unroll
                     for (int k = 0; k < kPass; ++k) {
                         const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
                         if (idx < a.g * D) {
+                            float Oown = 0.f;
+                            if (own >= 0) {
+#pragma unroll
+                                for (int wv = 0; wv < kConsumerWarps; ++wv)
+                                    Oown = __fmaf_rn(sm_m[wv * kGroupPad + h],
+                                                     sm_o[(wv * kGroupPad + h) * D + d], Oown);
+                            }
                             float O = 0.f;
 #pragma unroll
                             for (int i = 0; i < kConsumerWarps; ++i)
-                                if (i < nrec) O += sm_m[i * kGroupPad + h] * x[i][k];
-                            const float Lsum = sm_l[h];
+                                if (i < nrec)
+                                    O = __fmaf_rn(sm_pm[i * kGroupPad + h], i == own ? Oown : x[i][k],
+                                                  O);
+                            const float Lsum = sm_pl[h];
                             a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
                                 __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
                         }
                     }
                 }
                 if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
-            } else if (sm_flag[0]) {
-                // More pieces (a long pair over a narrow grid): one element at
-                // a time.
-                __threadfence();
+            } else if (merge) {
+                // More pieces (a long pair over a narrow grid), from the
+                // records: one element at a time.
                 for (int idx = tid; idx < a.g * D; idx += kCons) {
                     const int h = idx / D, d = idx - (idx / D) * D;
-                    float M = -INFINITY;
-                    for (int c = c_first; c <= c_last; ++c) {
+                    auto rec_of = [&](int c) -> const float * {
                         const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                        const float *r = a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
-                        M = fmaxf(M, __ldcg(r + D));
-                    }
+                        return a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                    };
+                    float M = -INFINITY;
+                    for (int c = c_first; c <= c_last; ++c) M = fmaxf(M, __ldcg(rec_of(c) + D));
                     float O = 0.f, Lsum = 0.f;
-                    if (M != -INFINITY) {
-                        for (int c = c_first; c <= c_last; ++c) {
-                            const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                            const float *r =
-                                a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
-                            const float f = ex2(__ldcg(r + D) - M);
-                            Lsum += f * __ldcg(r + D + 1);
-                            O += f * __ldcg(r + d);
-                        }
+                    for (int c = c_first; c <= c_last; ++c) {
+                        const float *r = rec_of(c);
+                        const float f = piece_factor(__ldcg(r + D), M);
+                        Lsum = __fmaf_rn(f, __ldcg(r + D + 1), Lsum);
+                        O = __fmaf_rn(f, __ldcg(r + d), O);
                     }
                     a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
                         __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
@@ -752,8 +916,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 1)
                 if (tid == 0) a.counters[s * a.Hk + kvh] = 0;
             }
         }
-        named_barrier_sync(1, kCons);  // the smem merge area is free again
-        pos += nb;
+        pos += sg.nu;
         if (abort) break;
     }
 }
@@ -763,7 +926,7 @@ size_t decode_smem_bytes(int B) {
     return 1024 + (size_t)NSTAGE * Layout<D, I8>::kStageBytes +
            (size_t)NSTAGE * Layout<D, I8>::kScaleBytes + Layout<D, I8>::kQsmBytes +
            2 * NSTAGE * sizeof(uint64_t) +
-           NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 2) * sizeof(float) +
+           NSTAGE * sizeof(int) + (size_t)kConsumerWarps * kGroupPad * (D + 4) * sizeof(float) +
            4 * sizeof(int) + 8 + (size_t)(B + 1) * sizeof(int64_t);
 }
 

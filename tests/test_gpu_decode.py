@@ -148,8 +148,8 @@ def test_decode_bad_context_is_reported():
 @pytest.mark.parametrize("ctxs,Hk,ctas,g,d", [
     ([2000, 3000], 2, 3, 4, 64), ([5000], 1, 5, 4, 64), ([3, 7000, 40, 900, 16], 2, 7, 4, 64),
     ([300, 20], 2, 1, 4, 64), ([1], 1, 2, 4, 64),
-    # head_dim 128, full groups: 2, 4 (the last pieces' one-pass merge, two
-    # passes of loads at fp16) and 5 pieces (element by element)
+    # head_dim 128, full groups: 2, 4 (the merge of up to four pieces, their
+    # records' loads in one pass at fp16) and 5 pieces (element by element)
     ([3000], 1, 2, 8, 128), ([5000], 1, 4, 8, 128), ([5000], 1, 5, 8, 128),
     ([4100, 100], 8, 3, 8, 128)])
 def test_decode_narrow_grid_merges_pieces(ctxs, Hk, ctas, g, d):
