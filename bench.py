@@ -6,9 +6,12 @@
 A step is one pass of the hot path over one batch of synthetic input.  For a
 decode workload: RoPE of the new tokens' Q/K + append of their K/V through
 slot_mapping (pa_rope_kv_write) and decode attention of every sequence
-against its whole cache (pa_decode).  For the prefill workload: RoPE + append
-of the new tokens and varlen causal prefill reading the cached prefix
-through block_tables (pa_prefill_varlen).
+against its whole cache (pa_decode), as the one call pa_decode_step (the two
+kernels chained by programmatic dependent launch).  For the prefill
+workload: RoPE + append of the new tokens and varlen causal prefill reading
+the cached prefix through block_tables (pa_prefill_varlen), as the one call
+pa_prefill_step.  The int8 cache has no one-call step: its steps are the two
+calls.
 
 The headline workload is the Llama-2-70B-shaped GQA decode (64 Q heads over
 8 KV heads, d=128, batch 32, 4096 cached tokens + 1); its metric is decode
@@ -24,8 +27,10 @@ Timing: W untimed warm-up steps, then exactly K steps between a barrier +
 synchronize on each side, CUDA events on the launching stream; the KV bytes
 a step reads (0.54 to 5.0 GB; 0.28 GB and up for the int8 cache) are larger
 than the 129 MB L2 (inputs larger than L2; no flush between steps).  The
-line gives the mean and the median step time.  Per-kernel durations of the dominant kernel come from events around
-its launches inside the same timed loop.  `e2e` repeats the step through the
+line gives the mean and the median step time.  Per-kernel durations (the
+dominant kernel against its roofline, the RoPE/append kernel's bandwidth)
+come from a second timed loop of the same K steps made of the two separate
+calls with events around each kernel.  `e2e` repeats the step through the
 library's calls with the step's inputs copied from pinned host memory (one
 copy of a buffer that holds them all) and the output copied back inside the
 timed region; for fp16 decode the step runs as the captured step graph with
@@ -251,6 +256,12 @@ class DecodeBench:
         if ev is not None:
             ev[2].record()
 
+    def fused_step(self):
+        """The step as one call (pa_decode_step: the two kernels chained)."""
+        pa, d, wl = self.pa, self.d, self.case.wl
+        pa.decode_step(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table, self.cache,
+                       d["bt"], d["ctx"], self.ws, wl.n_kv_heads, out=self.out, status=self.status)
+
     def e2e_setup(self):
         """Inputs from pinned host memory (one copy), the step, output back
         to pinned host memory.  Where there is a captured step graph, both
@@ -273,7 +284,7 @@ class DecodeBench:
             self.e2e_graph.launch()
             return
         self.packed.upload()
-        self.step()
+        self.fused_step()
         self.out_host.copy_(self.out, non_blocking=True)
 
     def e2e_close(self):
@@ -326,6 +337,10 @@ class DecodeI8Bench(DecodeBench):
         if ev is not None:
             ev[2].record()
 
+    def fused_step(self):
+        """No one-call int8 step: the two calls."""
+        self.step()
+
     def kernel_name(self):
         return "decode_kernel (int8 cache)"
 
@@ -377,6 +392,13 @@ class PrefillBench:
         if ev is not None:
             ev[2].record()
 
+    def fused_step(self):
+        """The step as one call (pa_prefill_step: the two kernels chained)."""
+        pa, d, wl = self.pa, self.d, self.case.wl
+        pa.prefill_step(d["q"], d["k"], d["v"], d["positions"], d["slots"], self.table, self.cache,
+                        d["cuq"], d["cuk"], d["bt"], self.md["max_seqlen_q"], wl.n_kv_heads,
+                        out=self.out, status=self.status)
+
     def e2e_setup(self):
         torch = self.torch
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
@@ -384,7 +406,7 @@ class PrefillBench:
 
     def e2e_step(self):
         self.packed.upload()
-        self.step()
+        self.fused_step()
         self.out_host.copy_(self.out, non_blocking=True)
 
     def e2e_close(self):
@@ -438,28 +460,38 @@ def rate(units, seconds, unit):
 
 
 def time_bench(b, steps, warmup, dist_ctx):
-    """Times `steps` steps after `warmup` untimed ones.  Returns (ms per step
-    over the whole timed region, max over ranks), the mean and median of
-    each step's own duration, of the attention kernel's and of the
-    RoPE/append kernel's (CUDA events on the launching stream around every
-    launch), and the device status word."""
+    """Times `steps` steps after `warmup` untimed ones, twice.  First the step
+    as a user runs it (one call: RoPE/append and the attention kernel
+    chained), with CUDA events only between steps: ms per step over the whole
+    timed region (max over ranks) and the mean and median of each step's own
+    duration.  Then the same steps made of the two separate calls with
+    events around each kernel (which keeps the kernels from overlapping):
+    the attention kernel's and the RoPE/append kernel's durations.  Returns
+    those and the device status word."""
     torch = b.torch
     for _ in range(warmup):
-        b.step()
+        b.fused_step()
     torch.cuda.synchronize()
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    kev = [(E(), E(), E()) for _ in range(steps)]
-    stop = E()
+    starts = [E() for _ in range(steps + 1)]
     dist_ctx.barrier()
     torch.cuda.synchronize()
     for i in range(steps):
-        b.step(kev[i])
-    stop.record()
+        starts[i].record()
+        b.fused_step()
+    starts[steps].record()
     torch.cuda.synchronize()
     dist_ctx.barrier()
-    ms = kev[0][0].elapsed_time(stop) / steps
-    starts = [e[0] for e in kev] + [stop]
+    ms = starts[0].elapsed_time(starts[steps]) / steps
     step_ms = [starts[i].elapsed_time(starts[i + 1]) for i in range(steps)]
+    # the kernels one at a time
+    for _ in range(warmup):
+        b.step()
+    kev = [(E(), E(), E()) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        b.step(kev[i])
+    torch.cuda.synchronize()
     kern = [z.elapsed_time(w) for _, z, w in kev]
     rope = [a.elapsed_time(z) for a, z, _ in kev]
     st = int(b.status.item())

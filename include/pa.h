@@ -302,6 +302,30 @@ int pa_decode_step(void *q, void *k, const void *v, const int32_t *positions,
                    size_t workspace_bytes, void *out, int32_t *dev_status, pa_stream_t stream);
 
 /*
+ * One prefill step of a batch in one call: pa_rope_kv_write of the batch's
+ * total_q new tokens followed by pa_prefill_varlen over them, chained as in
+ * pa_decode_step (the prefill kernel's set-up overlaps the RoPE/append
+ * kernel; it waits for the append's writes before it reads Q or the cache).
+ * The prefill of "nano-vllm notes - Llama" (prepare_prefill: positions,
+ * cu_seqlens, slot_mapping, then the varlen attention call) does these two
+ * things for every batch of new prompts or prompt chunks.
+ *   q, k, v            device fp16 [total_q][n_heads | n_kv_heads][head_dim]
+ *                      (q and k rotated in place)
+ *   positions, slot_mapping   device int32 [total_q]
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [num_seqs + 1]
+ * Every other argument, the results and the device-side checks are those of
+ * pa_rope_kv_write (num_tokens = total_q) and pa_prefill_varlen; the first
+ * error stops the call.  Allocates nothing and never synchronises.
+ */
+int pa_prefill_step(void *q, void *k, const void *v, const int32_t *positions,
+                    const int32_t *slot_mapping, const void *rope_table, int max_positions,
+                    const pa_cache_t *cache, int layer, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_k, const int32_t *block_tables,
+                    int max_blocks_per_seq, int num_seqs, int total_q, int max_seqlen_q,
+                    int n_heads, int n_kv_heads, int head_dim, float scale, void *out,
+                    int32_t *dev_status, pa_stream_t stream);
+
+/*
  * A decode step captured once into an executable CUDA graph and replayed
  * per step: pa_step_graph_create records pa_decode_step with the given
  * arguments (on a stream of its own, in relaxed capture mode) and

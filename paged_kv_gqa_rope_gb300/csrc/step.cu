@@ -1,7 +1,8 @@
 // A whole decode step behind one call (RoPE/append then decode, chained by
 // programmatic dependent launch) and its capture into a replayable CUDA
 // graph ("nano-vllm notes - Llama": the serving loop's decode step, captured
-// in a CUDA graph).
+// in a CUDA graph); the prefill step likewise (RoPE/append then the varlen
+// causal prefill, "nano-vllm notes - Llama", prepare_prefill).
 #include <cuda_runtime.h>
 
 #include <new>
@@ -27,6 +28,23 @@ extern "C" int pa_decode_step(void *q, void *k, const void *v, const int32_t *po
     return pa_decode(q, cache, layer, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      n_heads, n_kv_heads, head_dim, scale, workspace, workspace_bytes, out,
                      dev_status, stream);
+}
+
+extern "C" int pa_prefill_step(void *q, void *k, const void *v, const int32_t *positions,
+                               const int32_t *slot_mapping, const void *rope_table,
+                               int max_positions, const pa_cache_t *cache, int layer,
+                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                               const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+                               int total_q, int max_seqlen_q, int n_heads, int n_kv_heads,
+                               int head_dim, float scale, void *out, int32_t *dev_status,
+                               pa_stream_t stream) {
+    int rc = pa_rope_kv_write(q, k, v, positions, slot_mapping, total_q, n_heads, n_kv_heads,
+                              head_dim, rope_table, max_positions, cache, layer, dev_status,
+                              stream);
+    if (rc != PA_OK) return rc;
+    return pa_prefill_varlen(q, total_q, cache, layer, cu_seqlens_q, cu_seqlens_k, block_tables,
+                             max_blocks_per_seq, num_seqs, max_seqlen_q, n_heads, n_kv_heads,
+                             head_dim, scale, out, dev_status, stream);
 }
 
 namespace {

@@ -24,7 +24,8 @@ EXPORTS = (
     "pa_cache_bytes", "pa_alloc_cache", "pa_free_cache", "pa_prepare_prefill",
     "pa_prepare_decode", "pa_rope_table_bytes", "pa_rope_table_init", "pa_rope_kv_write",
     "pa_prefill_varlen", "pa_decode_workspace_bytes", "pa_decode", "pa_strerror",
-    "pa_check_device", "pa_decode_noalloc", "pa_decode_step", "pa_step_graph_create",
+    "pa_check_device", "pa_decode_noalloc", "pa_decode_step", "pa_prefill_step",
+    "pa_step_graph_create",
     "pa_step_graph_launch", "pa_step_graph_destroy", "pa_step_graph_create_io",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_blocks_needed", "pa_bm_allocate",
     "pa_bm_next_chunk", "pa_bm_mark_computed", "pa_bm_can_append", "pa_bm_append",
@@ -78,6 +79,9 @@ _SIGS = {
     "pa_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(PaCache), _i32,
                               _vp, _i32, _vp, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _sz,
                               _vp, _vp, _vp]),
+    "pa_prefill_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(PaCache), _i32,
+                               _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                               ctypes.c_float, _vp, _vp, _vp]),
     "pa_step_graph_create": (_i32, [ctypes.POINTER(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                     ctypes.POINTER(PaCache), _i32, _vp, _i32, _vp, _i32, _i32,
                                     _i32, _i32, ctypes.c_float, _vp, _sz, _vp, _vp]),
@@ -308,6 +312,27 @@ def prefill_varlen(q, cache: Cache, cu_seqlens_q, cu_seqlens_k, block_tables, ma
         _p(q), T, ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
         _p(block_tables), block_tables.shape[1], B, int(max_seqlen_q), H,
         n_kv_heads, d, float(scale), _p(out), _p(status), _stream(stream)))
+    return out
+
+
+def prefill_step(q, k, v, positions, slot_mapping, rope_table, cache: Cache, cu_seqlens_q,
+                 cu_seqlens_k, block_tables, max_seqlen_q, n_kv_heads, layer=0, scale=0.0,
+                 out=None, status=None, stream=None):
+    """pa_prefill_step: RoPE + append of the new tokens, then the varlen prefill."""
+    T, H, Hk, d = _rope_args(q, k, v, positions, slot_mapping, rope_table, status)
+    _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q", (None,))
+    B = cu_seqlens_q.shape[0] - 1
+    _dev(cu_seqlens_k, torch.int32, "cu_seqlens_k", (B + 1,))
+    _dev(block_tables, torch.int32, "block_tables", (B, None))
+    _table_width(block_tables)
+    if Hk != n_kv_heads:
+        raise ValueError(f"k has {Hk} KV heads, n_kv_heads is {n_kv_heads}")
+    out = _out(out, q)
+    _check("pa_prefill_step", lib().pa_prefill_step(
+        _p(q), _p(k), _p(v), _p(positions), _p(slot_mapping), _p(rope_table),
+        rope_table.shape[0], ctypes.byref(cache.desc), layer, _p(cu_seqlens_q), _p(cu_seqlens_k),
+        _p(block_tables), block_tables.shape[1], B, T, int(max_seqlen_q), H, n_kv_heads, d,
+        float(scale), _p(out), _p(status), _stream(stream)))
     return out
 
 

@@ -249,3 +249,23 @@ def test_prefill_repeats_bit_for_bit(shape):
     if shape == "skips":
         _, _, want, _ = oracle_prefill(case, init)
         assert_attention_close(first, want)
+
+
+def test_prefill_step_equals_separate_calls():
+    """pa_prefill_step (RoPE/append and the prefill chained in one call) gives
+    the bits of the two calls made one after the other, and the oracle's
+    attention within the tolerance."""
+    case, init = custom_prefill_case(16, 4, 128, [0, 37, 300], [513, 129, 1], seed=63)
+    sep = PrefillRun(case, init)
+    want = sep.run()
+    one = PrefillRun(case, init)
+    got = pa.prefill_step(one.q, one.k, one.v, one.pos, one.slots, one.table, one.cache, one.cuq,
+                          one.cuk, one.bt, one.md["max_seqlen_q"], case.wl.n_kv_heads,
+                          status=one.status)
+    torch.cuda.synchronize()
+    assert int(one.status.item()) == 0
+    assert torch.equal(got, want)
+    assert torch.equal(one.cache.tensor, sep.cache.tensor)
+    assert torch.equal(one.q, sep.q)
+    _, _, want64, _ = oracle_prefill(case, init)
+    assert_attention_close(got, want64)
