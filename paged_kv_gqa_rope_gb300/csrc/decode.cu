@@ -207,7 +207,22 @@ __device__ __forceinline__ void merge_factors(float *m, float *l, int h, int n) 
     l[kGroupPad + h] = M;
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// 16-byte asynchronous copy global -> shared through L2 only (the source is
+// written by other CTAs of the launch), and the wait for this thread's.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -822,68 +837,141 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
                 // Pieces i = 0 .. nrec-1 of the pair (CTA c_first + i), from
                 // their records, except this CTA's own when it closes the pair:
                 // (max, sum) per head from the merge factors above, O from the
-                // four warps' partial O.  Each thread loads the records' O
-                // values of its elements first, then their (max, sum), so the
-                // loads overlap.
-                const int own = close ? cta - c_first : -1;
-                // Elements tid + k * kCons, in one pass (fp16) or passes of
-                // two (int8, whose registers are capped for four CTAs per SM).
-                constexpr int kEl = kGroupPad * D / kCons;
-                constexpr int kPass = I8 && kEl > 2 ? 2 : kEl;
+                // four warps' partial O.
+                if constexpr (!I8) {
+                    // fp16: each thread loads the records' O values of its
+                    // elements into registers first, then their (max, sum), so
+                    // the loads overlap.
+                    const int own = close ? cta - c_first : -1;
+                    constexpr int kEl = kGroupPad * D / kCons;
+                    constexpr int kPass = kEl;
 #pragma unroll 1
-                for (int k0 = 0; k0 < kEl; k0 += kPass) {
-                    float x[kConsumerWarps][kPass];
+                    for (int k0 = 0; k0 < kEl; k0 += kPass) {
+                        float x[kConsumerWarps][kPass];
 #pragma unroll
-                    for (int i = 0; i < kConsumerWarps; ++i) {
-                        const int c = c_first + i;
-                        const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                        const float *pb = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
+                        for (int i = 0; i < kConsumerWarps; ++i) {
+                            const int c = c_first + i;
+                            const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                            const float *pb = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
+#pragma unroll
+                            for (int k = 0; k < kPass; ++k) {
+                                const int idx = tid + (k0 + k) * kCons, h = idx / D,
+                                          d = idx - h * D;
+                                x[i][k] = i < nrec && i != own && idx < a.g * D
+                                              ? __ldcg(pb + h * L::kRec + d)
+                                              : 0.f;
+                            }
+                        }
+                        if (k0 == 0) {
+                            if (tid < nrec * a.g) {
+                                const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
+                                float pm, pl;
+                                if (i == own) {
+                                    pm = sm_l[kGroupPad + h];
+                                    pl = sm_l[h];
+                              } else {
+                                    const int c = c_first + i;
+                                    const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                                    const float *r =
+                                        a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                                    pm = __ldcg(r + D);
+                                    pl = __ldcg(r + D + 1);
+                                }
+                                sm_pm[i * kGroupPad + h] = pm;
+                                sm_pl[i * kGroupPad + h] = pl;
+                            }
+                            named_barrier_sync(1, kCons);
+                            if (tid < a.g) merge_factors(sm_pm, sm_pl, tid, nrec);
+                            named_barrier_sync(1, kCons);
+                        }
 #pragma unroll
                         for (int k = 0; k < kPass; ++k) {
                             const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
-                            x[i][k] = i < nrec && i != own && idx < a.g * D
-                                          ? __ldcg(pb + h * L::kRec + d)
-                                          : 0.f;
-                        }
-                    }
-                    if (k0 == 0) {
-                        if (tid < nrec * a.g) {
-                            const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
-                            float pm, pl;
-                            if (i == own) {
-                                pm = sm_l[kGroupPad + h];
-                                pl = sm_l[h];
-                            } else {
-                                const int c = c_first + i;
-                                const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
-                                const float *r =
-                                    a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
-                                pm = __ldcg(r + D);
-                                pl = __ldcg(r + D + 1);
-                            }
-                            sm_pm[i * kGroupPad + h] = pm;
-                            sm_pl[i * kGroupPad + h] = pl;
-                        }
-                        named_barrier_sync(1, kCons);
-                        if (tid < a.g) merge_factors(sm_pm, sm_pl, tid, nrec);
-                        named_barrier_sync(1, kCons);
-                    }
+                            if (idx < a.g * D) {
+                                float Oown = 0.f;
+                                if (own >= 0) {
 #pragma unroll
-                    for (int k = 0; k < kPass; ++k) {
-                        const int idx = tid + (k0 + k) * kCons, h = idx / D, d = idx - h * D;
+                                    for (int wv = 0; wv < kConsumerWarps; ++wv)
+                                        Oown = __fmaf_rn(sm_m[wv * kGroupPad + h],
+                                                         sm_o[(wv * kGroupPad + h) * D + d], Oown);
+                                }
+                                float O = 0.f;
+#pragma unroll
+                                for (int i = 0; i < kConsumerWarps; ++i)
+                                    if (i < nrec)
+                                        O = __fmaf_rn(sm_pm[i * kGroupPad + h],
+                                                      i == own ? Oown : x[i][k], O);
+                                const float Lsum = sm_pl[h];
+                                a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
+                                    __float2half_rn(Lsum > 0.f ? O / Lsum : 0.f);
+                            }
+                        }
+                    }
+                  } else {
+                    // int8 (registers capped for four CTAs per SM): this CTA's own
+                    // O goes to registers first; the records' O rows are then
+                    // copied into the partial-O area (piece i's g rows where warp
+                    // i's were) by asynchronous copies, one round trip for all of
+                    // them, beside the loads of their (max, sum).
+                    const int own = close ? cta - c_first : -1;
+                    constexpr int kEl = kGroupPad * D / kCons;
+                    float oown[kEl];
+#pragma unroll
+                    for (int k = 0; k < kEl; ++k) {
+                        const int idx = tid + k * kCons, h = idx / D, d = idx - h * D;
+                        oown[k] = 0.f;
+                        if (own >= 0 && idx < a.g * D) {
+#pragma unroll
+                            for (int wv = 0; wv < kConsumerWarps; ++wv)
+                                oown[k] = __fmaf_rn(sm_m[wv * kGroupPad + h],
+                                                    sm_o[(wv * kGroupPad + h) * D + d], oown[k]);
+                        }
+                    }
+                    named_barrier_sync(1, kCons);  // the partial O is read: its area is free
+                    constexpr int kChunks = D / 4;  // 16-byte pieces of a row
+                    for (int i = 0; i < nrec; ++i) {
+                        if (i == own) continue;
+                        const int c = c_first + i;
+                        const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                        const float *pb = a.rec + (int64_t)(c * 2 + sl) * kGroupPad * L::kRec;
+                        for (int ch = tid; ch < a.g * kChunks; ch += kCons) {
+                            const int h = ch / kChunks, d = (ch - h * kChunks) * 4;
+                            cp_async16(sm_o + (i * kGroupPad + h) * D + d, pb + h * L::kRec + d);
+                        }
+                    }
+                    cp_async_commit();
+                    if (tid < nrec * a.g) {
+                        const int i = tid / a.g, h = tid - (tid / a.g) * a.g;
+                        float pm, pl;
+                        if (i == own) {
+                            pm = sm_l[kGroupPad + h];
+                            pl = sm_l[h];
+                        } else {
+                            const int c = c_first + i;
+                            const int sl = sg.pair_start <= range_start(W, c, G) ? 0 : 1;
+                            const float *r =
+                                a.rec + ((int64_t)(c * 2 + sl) * kGroupPad + h) * L::kRec;
+                            pm = __ldcg(r + D);
+                            pl = __ldcg(r + D + 1);
+                        }
+                        sm_pm[i * kGroupPad + h] = pm;
+                        sm_pl[i * kGroupPad + h] = pl;
+                    }
+                    cp_async_wait_all();
+                    named_barrier_sync(1, kCons);
+                    if (tid < a.g) merge_factors(sm_pm, sm_pl, tid, nrec);
+                    named_barrier_sync(1, kCons);
+#pragma unroll
+                    for (int k = 0; k < kEl; ++k) {
+                        const int idx = tid + k * kCons, h = idx / D, d = idx - h * D;
                         if (idx < a.g * D) {
-                            float Oown = 0.f;
-                            if (own >= 0) {
-#pragma unroll
-                                for (int wv = 0; wv < kConsumerWarps; ++wv)
-                                    Oown = __fmaf_rn(sm_m[wv * kGroupPad + h],
-                                                     sm_o[(wv * kGroupPad + h) * D + d], Oown);
-                            }
                             float O = 0.f;
 #pragma unroll
                             for (int i = 0; i < kConsumerWarps; ++i)
                                 if (i < nrec)
-                                    O = __fmaf_rn(sm_pm[i * kGroupPad + h], i == own ? Oown : x[i][k],
+                                    O = __fmaf_rn(sm_pm[i * kGroupPad + h],
+                                                  i == own ? oown[k]
+                                                           : sm_o[(i * kGroupPad + h) * D + d],
                                                   O);
                             const float Lsum = sm_pl[h];
                             a.out[((int64_t)s * a.H + kvh * a.g + h) * D + d] =
