@@ -5,18 +5,19 @@
 // "Meta Llama source deep-dive", 3.4 repeat_kv: Q head h reads KV head h/g).
 //
 // Work decomposition.  Every (sequence s, KV head h) pair owns
-// ceil(context_lens[s] / 16) KV blocks followed by kPairCost units that
-// stand for the pair's fixed cost (its merge and output, about the time of
-// four blocks' streaming); laid end to end, pair after pair, they form one
-// line of W units.  The persistent grid of G CTAs cuts that line into G equal
-// ranges, so every CTA has about the same work whatever the mix of context
-// lengths (a CTA with many short pairs streams fewer blocks).  A CTA walks
-// its range as segments (the part of one pair that falls in it; a segment
-// of a pair's cost units alone has no block and is skipped).  A pair whose
-// blocks lie inside one range is finished there; a pair whose blocks are cut
-// by range ends is finished by the CTA that completes its last piece: each
-// piece leaves (max, sum, unnormalised O) in the workspace (record slot 0 if
-// it is the CTA's first segment, 1 if its last), and the last to arrive
+// ceil(context_lens[s] / 16) KV blocks and a few units (after them; before
+// them in the int8 kernel) that stand for the pair's fixed cost (its merge
+// and output, about the time of four fp16 or eight int8 blocks' streaming);
+// laid end to end, pair after pair, they form one line of W units.  The
+// persistent grid of G CTAs cuts that line into G equal ranges, so every CTA
+// has about the same work whatever the mix of context lengths (a CTA with
+// many short pairs streams fewer blocks).  A CTA walks its range as segments (the part of one pair that
+// falls in it; a segment of a pair's cost units alone has no block and is
+// skipped).  A pair whose blocks lie inside one range is finished there; a
+// pair whose blocks are cut by range ends is finished by the CTA that
+// completes its last piece: each piece leaves (max, sum, unnormalised O) in
+// the workspace (record slot 0 if the pair's blocks began before the CTA's
+// range, 1 if they begin in it and go on past it), and the last to arrive
 // merges the 2-3 pieces by an online softmax and resets the pair's arrival
 // counter to zero; if the pieces of the others have all arrived when a CTA
 // reaches the end of its last segment, that CTA closes the pair from its own
@@ -100,18 +101,27 @@ __device__ __forceinline__ int cta_of(int64_t idx, int64_t W, int G) {
     return (int)(((idx + 1) * G + W - 1) / W) - 1;
 }
 
-// Units of the line that stand for one pair's fixed cost.
+// Units of the line that stand for one pair's fixed cost: four after its
+// blocks for the fp16 kernel, eight before them for the int8 kernel (whose
+// blocks stream twice as fast and whose merges cost more of them).  Before
+// its blocks, the units fall to the CTA that holds the pair's first block,
+// the CTA that closes or merges a cut pair at the end of its range: that
+// measured better for the int8 kernel (ragged_decode 485 -> 463 us), after
+// them better for the fp16 one (757 -> 753 us).
 constexpr int kPairCost = 4;
+constexpr int kPairCostI8 = 8;
 
 // Segment of the line starting at `pos` (< end): its pair, its nu units and
 // the nb blocks among them (blocks b0 .. b0 + nb - 1 of the pair, nb = 0 for
 // a segment of cost units alone); the pair's blocks are the units
-// [pair_start, pair_end).
+// [pair_start, pair_end), its kCost cost units before them (kFront) or
+// after them.
 struct Segment {
     int s, kvh, b0, nb, nu, ctx;
     int64_t pair_start, pair_end;
 };
 
+template <int kCost, bool kFront>
 __device__ __forceinline__ Segment segment_at(int64_t pos, int64_t end, const int64_t *prefix,
                                               int B, const int32_t *context_lens) {
     int lo = 0, hi = B - 1;  // largest s with prefix[s] <= pos
@@ -126,15 +136,18 @@ __device__ __forceinline__ Segment segment_at(int64_t pos, int64_t end, const in
     g.s = lo;
     g.ctx = __ldg(context_lens + lo);
     const int nblk = (g.ctx + kBlockSize - 1) / kBlockSize;
-    const int span = nblk + kPairCost;
+    const int span = kCost + nblk;
     const int64_t rem = pos - prefix[lo];
     g.kvh = (int)(rem / span);
     const int u0 = (int)(rem - (int64_t)g.kvh * span);  // unit of the pair
-    g.pair_start = prefix[lo] + (int64_t)g.kvh * span;
+    const int64_t base = prefix[lo] + (int64_t)g.kvh * span;
+    const int lead = kFront ? kCost : 0;  // units before the blocks
+    g.pair_start = base + lead;
     g.pair_end = g.pair_start + nblk;
-    g.nu = (int)(min(end, g.pair_start + span) - pos);
-    g.b0 = min(u0, nblk);
-    g.nb = max(0, min(u0 + g.nu, nblk) - u0);
+    g.nu = (int)(min(end, base + span) - pos);
+    const int first = max(u0, lead), last = min(u0 + g.nu, lead + nblk);  // units of blocks
+    g.nb = max(0, last - first);
+    g.b0 = min(first - lead, nblk);
     return g;
 }
 
@@ -306,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
     // has not consumed yet (the mbarrier parity would alias that wait onto
     // the earlier, completed phase).
     static_assert(NSTAGE % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
+    constexpr int kCost = I8 ? kPairCostI8 : kPairCost;
     using L = Layout<D, I8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
         const int ctx = __ldg(a.context_lens + s);
         int64_t n = 0;
         if (ctx >= 1 && ctx <= a.maxb * kBlockSize)
-            n = (int64_t)((ctx + kBlockSize - 1) / kBlockSize + kPairCost) * a.Hk;
+            n = (int64_t)((ctx + kBlockSize - 1) / kBlockSize + kCost) * a.Hk;
         else if (cta == 0)
             report(a.status, PA_DEV_BAD_LENGTH);
         prefix[s + 1] = n;
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
         int gblk = 0;
         bool abort = false;
         for (int64_t pos = start; pos < end && !abort;) {
-            const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
+            const Segment sg = segment_at<kCost, I8>(pos, end, prefix, B, a.context_lens);
             const int32_t *row = a.block_tables + (int64_t)sg.s * a.maxb + sg.b0;
             for (int w0 = 0; w0 < sg.nb && !abort; w0 += 32) {
                 const int cnt = min(32, sg.nb - w0);
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
     constexpr int kCons = kConsumerWarps * 32;
     int gblk = 0;
     for (int64_t pos = start; pos < end;) {
-        const Segment sg = segment_at(pos, end, prefix, B, a.context_lens);
+        const Segment sg = segment_at<kCost, I8>(pos, end, prefix, B, a.context_lens);
         const int s = sg.s, kvh = sg.kvh, b0 = sg.b0, nb = sg.nb, ctx = sg.ctx;
         if (nb == 0) {  // cost units alone
             pos += sg.nu;
@@ -741,7 +755,10 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
                 ow[D + d + 8] = o[mt][3];
             }
         }
-        const bool whole = pos == sg.pair_start && pos + nb == sg.pair_end;
+        // (a whole pair's segment starts at the pair's first block unless
+        // cost units come before the blocks)
+        const bool whole = I8 ? b0 == 0 && b0 + nb == sg.pair_end - sg.pair_start
+                              : pos == sg.pair_start && pos + nb == sg.pair_end;
         // A cut pair: its pieces are those of CTAs c_first .. c_last.  On the
         // CTA's last segment, if every other piece has already arrived on the
         // pair's counter, this piece is the last, and the pair is merged from
@@ -785,7 +802,9 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
             // record stores); the piece that arrives last merges the pair.
             bool merge = close;
             if (!close) {
-                const int slot = pos == start ? 0 : 1;
+                // slot 0 for a pair whose blocks began before this range (with
+                // cost units after the blocks: this CTA's first segment)
+                const int slot = (I8 ? sg.pair_start <= start : pos == start) ? 0 : 1;
                 float *myrec = a.rec + ((int64_t)(cta * 2 + slot) * kGroupPad) * L::kRec;
                 for (int idx = tid; idx < a.g * D; idx += kCons) {
                     const int h = idx / D, d = idx - (idx / D) * D;
