@@ -7,7 +7,7 @@
 // Work decomposition.  Every (sequence s, KV head h) pair owns
 // ceil(context_lens[s] / 16) KV blocks and a few units (after them; before
 // them in the int8 kernel) that stand for the pair's fixed cost (its merge
-// and output, about the time of four fp16 or eight int8 blocks' streaming);
+// and output, about the time of ten fp16 or eight int8 blocks' streaming);
 // laid end to end, pair after pair, they form one line of W units.  The
 // persistent grid of G CTAs cuts that line into G equal ranges, so every CTA
 // has about the same work whatever the mix of context lengths (a CTA with
@@ -101,14 +101,16 @@ __device__ __forceinline__ int cta_of(int64_t idx, int64_t W, int G) {
     return (int)(((idx + 1) * G + W - 1) / W) - 1;
 }
 
-// Units of the line that stand for one pair's fixed cost: four after its
+// Units of the line that stand for one pair's fixed cost: ten after its
 // blocks for the fp16 kernel, eight before them for the int8 kernel (whose
 // blocks stream twice as fast and whose merges cost more of them).  Before
 // its blocks, the units fall to the CTA that holds the pair's first block,
 // the CTA that closes or merges a cut pair at the end of its range: that
 // measured better for the int8 kernel (ragged_decode 485 -> 463 us), after
-// them better for the fp16 one (757 -> 753 us).
-constexpr int kPairCost = 4;
+// them better for the fp16 one (757 -> 753 us).  fp16 ragged_decode took
+// 753, 740 and 742 us with 4, 10 and 16 units (gqa_decode_70b 88.6, 88.6
+// and 89.4 us; mha_decode_7b 164.8, 164.4 and 164.5 us).
+constexpr int kPairCost = 10;
 constexpr int kPairCostI8 = 8;
 
 // Segment of the line starting at `pos` (< end): its pair, its nu units and
