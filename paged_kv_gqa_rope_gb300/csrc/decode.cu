@@ -176,12 +176,33 @@ __device__ __forceinline__ uint32_t code_offset(int r, int c) {
 
 // 4-D tiled load (the int8 code map) into shared memory.
 __device__ __forceinline__ void tma_load_4d_u8(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int c0, int c1, int c2, int c3) {
+                                               int c0, int c1, int c2, int c3, uint64_t pol) {
     asm volatile(
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-        "r"(smem_u32(bar))
+        "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// L2 policy for data read once: its lines are the first to go, so that the
+// small data read by every launch (context lengths, block tables, Q, the
+// pieces' records) stays in L2 while the cache streams through.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 5-D tiled load (the fp16 cache map) into shared memory with an L2 policy.
+__device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int c0, int c1, int c2, int c3, int c4,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 
@@ -399,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
         }
         int gblk = 0;
         bool abort = false;
+        const uint64_t pol = l2_evict_first();
         for (int64_t pos = start; pos < end && !abort;) {
             const Segment sg = segment_at<kCost, I8>(pos, end, prefix, B, a.context_lens);
             const int32_t *row = a.block_tables + (int64_t)sg.s * a.maxb + sg.b0;
@@ -423,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
                                 mbar_arrive_expect_tx(&full[stage],
                                                       L::kStageBytes + L::kScaleBytes);
                                 tma_load_4d_u8(dst, &kvmap, &full[stage], 0, sg.kvh,
-                                               blk * kBlockSize, 0);
+                                               blk * kBlockSize, 0, pol);
                                 tma_load_3d(scale_ring + stage * L::kScaleBytes, &smap,
                                             &full[stage], 0, blk * a.Hk + sg.kvh, 0);
                             } else {
                                 mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-                                tma_load_5d(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
-                                            blk * kBlockSize, 0);
+                                tma_load_5d_hint(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
+                                                 blk * kBlockSize, 0, pol);
                             }
                         } else {
                             report(a.status, PA_DEV_BAD_BLOCK);
