@@ -363,6 +363,11 @@ int pa_step_graph_destroy(pa_step_graph_t graph);
  * destroyed; the caller fills host_in before a replay and reads host_out
  * after it has completed (e.g. after synchronising the replay's stream).
  * in_bytes = 0 leaves out the input copy, host_out = NULL the output copy.
+ * Each copy is a small kernel that reads (or writes) the host buffer through
+ * its device mapping (page-locked memory is mapped under unified addressing)
+ * when the mapping exists and both addresses are 16-byte aligned, else a
+ * cudaMemcpyAsync; the graph's kernels are chained by programmatic
+ * dependent launch, each waiting for the one before it to finish.
  * Errors: those of pa_step_graph_create, and PA_ERR_INVALID for a missing
  * or pageable host buffer (nothing is created).
  */

@@ -208,11 +208,12 @@ __device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *m
 
 // 3-D tiled load (the int8 scale map) into shared memory.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int c0, int c1, int c2) {
+                                            int c0, int c1, int c2, uint64_t pol) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+        "l"(pol)
         : "memory");
 }
 
@@ -404,6 +405,11 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
     // Everything above read only call metadata; Q and the cache may still be
     // being written by the RoPE/append kernel before this one.
     griddep_wait();
+    // The kernel after this one (the next step's RoPE/append, the step
+    // graph's output copy) may be launched now: it waits for this grid to
+    // finish before it touches memory, and this grid's CTAs are all resident
+    // (one persistent wave), so its launch latency hides under this kernel.
+    griddep_launch_dependents();
     const int64_t W = prefix[B];
     // With fewer blocks than CTAs only the first W CTAs get a (one-block)
     // range, so that every range is non-empty and a pair cut into pieces
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
                                 tma_load_4d_u8(dst, &kvmap, &full[stage], 0, sg.kvh,
                                                blk * kBlockSize, 0, pol);
                                 tma_load_3d(scale_ring + stage * L::kScaleBytes, &smap,
-                                            &full[stage], 0, blk * a.Hk + sg.kvh, 0);
+                                            &full[stage], 0, blk * a.Hk + sg.kvh, 0, pol);
                             } else {
                                 mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
                                 tma_load_5d_hint(dst, &kvmap, &full[stage], 0, 0, sg.kvh,

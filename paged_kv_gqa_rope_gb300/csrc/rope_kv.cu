@@ -42,7 +42,12 @@ template <int D>
 __global__ void __launch_bounds__(kTokenThreads) rope_kv_write_kernel(const RopeArgs a) {
     // The decode or prefill kernel that follows may start its set-up now; it
     // waits (griddepcontrol.wait) for this kernel's writes before using them.
+    // This kernel is itself launched as a dependent: it reads and writes
+    // nothing before the kernel ahead of it (the previous step's attention
+    // kernel, which reads the cache and Q, or the step graph's input copy)
+    // has finished.
     griddep_launch_dependents();
+    griddep_wait();
     constexpr int kPieces = D / 8;  // 16-byte pieces per head row
     const int rows = a.n_heads + 2 * a.n_kv_heads;
     const int t = (int)(blockIdx.z * gridDim.y + blockIdx.y);
@@ -103,6 +108,7 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 template <int D>
 __global__ void __launch_bounds__(kTokenThreads) rope_kv_write_staged_kernel(const RopeArgs a) {
     griddep_launch_dependents();
+    griddep_wait();
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int kPieces = D / 8;
     const int H = a.n_heads, Hk = a.n_kv_heads, rows = H + 2 * Hk;
@@ -258,15 +264,17 @@ extern "C" int pa_rope_kv_write(void *q, void *k, const void *v, const int32_t *
         }
         const int grid = (int)std::min<int64_t>(num_tokens, (int64_t)sm_count() * per_sm);
         if (head_dim == 128)
-            rope_kv_write_staged_kernel<128><<<grid, kTokenThreads, smem, st>>>(a);
+            launch_dependent(rope_kv_write_staged_kernel<128>, dim3(grid), dim3(kTokenThreads),
+                             smem, st, a);
         else
-            rope_kv_write_staged_kernel<64><<<grid, kTokenThreads, smem, st>>>(a);
+            launch_dependent(rope_kv_write_staged_kernel<64>, dim3(grid), dim3(kTokenThreads),
+                             smem, st, a);
         return launch_status();
     }
     const dim3 grid = token_grid(num_tokens, (n_heads + 2 * n_kv_heads) * (head_dim / 8));
     if (head_dim == 128)
-        rope_kv_write_kernel<128><<<grid, kTokenThreads, 0, st>>>(a);
+        launch_dependent(rope_kv_write_kernel<128>, grid, dim3(kTokenThreads), 0, st, a);
     else
-        rope_kv_write_kernel<64><<<grid, kTokenThreads, 0, st>>>(a);
+        launch_dependent(rope_kv_write_kernel<64>, grid, dim3(kTokenThreads), 0, st, a);
     return launch_status();
 }

@@ -5,8 +5,12 @@
 // causal prefill, "nano-vllm notes - Llama", prepare_prefill).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
 #include <new>
 
+#include "common.cuh"
+#include "internal.h"
 #include "pa.h"
 
 struct pa_step_graph {
@@ -60,6 +64,48 @@ bool page_locked(const void *p) {
     return at.type == cudaMemoryTypeHost;
 }
 
+// The device's address of page-locked host memory mapped into its address
+// space (all cudaHostAlloc memory under unified addressing), else null.
+void *mapped_ptr(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// n bytes from src to dst (both 16-byte aligned), one 16-byte piece per
+// thread and pass, the last n % 16 bytes by block 0.  The step graph's
+// host <-> device copies: this kernel reads or writes the mapped host
+// buffer itself, so the copy is one kernel node instead of a copy-engine
+// transfer with its own set-up latency.  Launched as a dependent of the
+// kernel before it (whose writes it waits for) and letting the next one
+// launch at once.
+__global__ void __launch_bounds__(256)
+    copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n16,
+                const uint8_t *__restrict__ src_b, uint8_t *__restrict__ dst_b, size_t n) {
+    pa::griddep_launch_dependents();
+    pa::griddep_wait();
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        dst[i] = src[i];
+    if (blockIdx.x == 0)
+        for (size_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x) dst_b[i] = src_b[i];
+}
+
+int copy_by_kernel(const void *src, void *dst, size_t n, cudaStream_t st) {
+    const size_t n16 = n / 16;
+    const int blocks =
+        (int)std::max<size_t>(1, std::min<size_t>((n16 + 255) / 256, (size_t)pa::sm_count() * 4));
+    pa::launch_dependent(copy_kernel, dim3(blocks), dim3(256), 0, st,
+                         static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16,
+                         static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst), n);
+    return pa::launch_status();
+}
+
 }  // namespace
 
 extern "C" int pa_step_graph_create_io(
@@ -87,17 +133,29 @@ extern "C" int pa_step_graph_create_io(
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
         rc = PA_ERR_CUDA;
     } else {
-        if (in_bytes > 0 &&
-            cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
-            rc = PA_ERR_CUDA;
+        // The copies: a kernel on the mapped host buffer when there is one
+        // (and every address is 16-byte aligned), else a copy-engine copy.
+        if (in_bytes > 0) {
+            const void *src = mapped_ptr(host_in);
+            if (src && aligned16(src) && aligned16(dev_in))
+                rc = copy_by_kernel(src, dev_in, in_bytes, cs);
+            else if (cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, cs) !=
+                     cudaSuccess)
+                rc = PA_ERR_CUDA;
+        }
         if (rc == PA_OK)
             rc = pa_decode_step(q, k, v, positions, slot_mapping, rope_table, max_positions,
                                 cache, layer, block_tables, max_blocks_per_seq, context_lens,
                                 num_seqs, n_heads, n_kv_heads, head_dim, scale, workspace,
                                 workspace_bytes, out, dev_status, cs);
-        if (rc == PA_OK && out_bytes > 0 &&
-            cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
-            rc = PA_ERR_CUDA;
+        if (rc == PA_OK && out_bytes > 0) {
+            void *dst = mapped_ptr(host_out);
+            if (dst && aligned16(dst) && aligned16(out))
+                rc = copy_by_kernel(out, dst, out_bytes, cs);
+            else if (cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, cs) !=
+                     cudaSuccess)
+                rc = PA_ERR_CUDA;
+        }
         // End the capture whatever happened, so the stream is usable again.
         if (cudaStreamEndCapture(cs, &g) != cudaSuccess && rc == PA_OK) rc = PA_ERR_CUDA;
     }
