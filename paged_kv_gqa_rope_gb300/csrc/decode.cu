@@ -207,13 +207,15 @@ __device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *m
 }
 
 // 3-D tiled load (the int8 scale map) into shared memory.
+// (No evict-first policy here: a block's 64-byte scale rows of two KV heads
+// share a 128-byte L2 line, which the other head's copy then reads from L2;
+// with the policy the int8 kernels read the scales twice from DRAM.)
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int c0, int c1, int c2, uint64_t pol) {
+                                            int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-        "l"(pol)
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, I8 ? 4 : 2)
                                 tma_load_4d_u8(dst, &kvmap, &full[stage], 0, sg.kvh,
                                                blk * kBlockSize, 0, pol);
                                 tma_load_3d(scale_ring + stage * L::kScaleBytes, &smap,
-                                            &full[stage], 0, blk * a.Hk + sg.kvh, 0, pol);
+                                            &full[stage], 0, blk * a.Hk + sg.kvh, 0);
                             } else {
                                 mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
                                 tma_load_5d_hint(dst, &kvmap, &full[stage], 0, 0, sg.kvh,
