@@ -293,6 +293,13 @@ int pa_decode_noalloc(const void *q, const pa_cache_t *cache, int layer,
  * Every other argument, the results and the device-side checks are those of
  * pa_rope_kv_write (num_tokens = num_seqs) and pa_decode; the first error
  * stops the call.  Allocates nothing and never synchronises.
+ * Launch order: the RoPE/append kernel is launched as a programmatic
+ * dependent of the work before it in the stream (it waits for it to finish
+ * before touching memory), and lets the decode kernel start at once; the
+ * decode kernel reads context_lens and block_tables in its set-up, before
+ * its wait.  So the work that writes those two arrays must not let its
+ * dependents launch early (griddepcontrol.launch_dependents): a copy, or a
+ * kernel launched without that instruction, is what this library expects.
  */
 int pa_decode_step(void *q, void *k, const void *v, const int32_t *positions,
                    const int32_t *slot_mapping, const void *rope_table, int max_positions,

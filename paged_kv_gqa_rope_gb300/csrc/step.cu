@@ -82,12 +82,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // host <-> device copies: this kernel reads or writes the mapped host
 // buffer itself, so the copy is one kernel node instead of a copy-engine
 // transfer with its own set-up latency.  Launched as a dependent of the
-// kernel before it (whose writes it waits for) and letting the next one
-// launch at once.
+// kernel before it (whose writes it waits for).  It does not let the next
+// kernel launch early: the input copy writes the decode kernel's context
+// lengths and block tables, which that kernel reads before its own
+// grid-dependency wait, so the RoPE/append kernel between them must not
+// start (and let the decode kernel start) before this copy has finished.
 __global__ void __launch_bounds__(256)
     copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n16,
                 const uint8_t *__restrict__ src_b, uint8_t *__restrict__ dst_b, size_t n) {
-    pa::griddep_launch_dependents();
     pa::griddep_wait();
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)

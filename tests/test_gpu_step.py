@@ -102,14 +102,15 @@ def test_step_graph_launches_on_any_stream():
     assert torch.equal(out, want)
 
 
-def _packed(arrays):
+def _packed(arrays, host_offset=0):
     """Host arrays laid out in one pinned uint8 buffer (256-byte aligned
-    offsets) and device views of a device buffer of the same layout."""
+    offsets, the buffer itself starting host_offset bytes into a pinned
+    allocation) and device views of a device buffer of the same layout."""
     off, lay = 0, {}
     for k, a in arrays.items():
         lay[k] = (off, a)
         off = (off + a.nbytes + 255) // 256 * 256
-    host = torch.zeros(off, dtype=torch.uint8).pin_memory()
+    host = torch.zeros(off + 16, dtype=torch.uint8).pin_memory()[host_offset:host_offset + off]
     dev = torch.zeros(off, dtype=torch.uint8, device="cuda")
     views = {k: dev[o:o + a.nbytes].view(torch.from_numpy(a).dtype).view(a.shape)
              for k, (o, a) in lay.items()}
@@ -123,10 +124,14 @@ def _packed(arrays):
     return host, dev, views, fill
 
 
-def test_step_graph_with_host_io_replays_a_serving_loop():
+@pytest.mark.parametrize("host_offset", [0, 4], ids=["copy-kernels", "copy-engine"])
+def test_step_graph_with_host_io_replays_a_serving_loop(host_offset):
     """pa_step_graph_create_io: each replay copies the step's inputs from
     pinned host memory, runs RoPE/append + decode and copies the output
-    back; the device input buffers are never written any other way."""
+    back; the device input buffers are never written any other way.  With
+    16-byte aligned host buffers the copies are kernels reading and writing
+    the mapped host memory; 4 bytes off that alignment they are copy-engine
+    copies."""
     ctxs = [5, 100, 1000, 2999]
     case, init = custom_case(16, 4, 128, ctxs, seed=25)
     run = DecodeRun(case, init, table_rows=4096)
@@ -136,8 +141,12 @@ def test_step_graph_with_host_io_replays_a_serving_loop():
                                 slots=m["slot_mapping"].astype(np.int32),
                                 ctx=m["context_lens"].astype(np.int32),
                                 bt=c.block_tables.astype(np.int32))
-    host, dev, d, fill = _packed(step_in(case, md))
-    host_out = torch.zeros(tuple(run.q.shape), dtype=torch.float16).pin_memory()
+    host, dev, d, fill = _packed(step_in(case, md), host_offset)
+    n_out = run.q.numel()
+    host_out = torch.zeros(n_out + 8, dtype=torch.float16).pin_memory()[
+        host_offset // 2:host_offset // 2 + n_out].view(tuple(run.q.shape))
+    assert (host.data_ptr() % 16 == 0) == (host_offset == 0)
+    assert (host_out.data_ptr() % 16 == 0) == (host_offset == 0)
     g = pa.StepGraph(d["q"], d["k"], d["v"], d["positions"], d["slots"], run.table, run.cache,
                      d["bt"], d["ctx"], run.ws, case.wl.n_kv_heads, status=run.status,
                      host_in=host, dev_in=dev, host_out=host_out)
