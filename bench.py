@@ -370,6 +370,13 @@ class PrefillBench:
                          cuq=md["cu_seqlens_q"], cuk=md["cu_seqlens_k"])
         self.packed = PackedInputs(self.host, dev)
         self.d = self.packed.views
+        # the library's choice of RoPE/append kernel (a label only): the
+        # staged kernel for at least eight tokens per SM when two stages of
+        # a token's rows fit in its 100 KB of shared memory
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        stage = (wl.n_heads + 2 * wl.n_kv_heads) * wl.head_dim * 2
+        if len(case.q) >= 8 * sms and 2 * stage + 16 <= 100 * 1024:
+            self.rope_kernel = "rope_kv_write_staged_kernel"
         self.out = torch.empty_like(self.d["q"])
         self.status = pa.new_status(dev)
         self.units = prefill_flops(case)
